@@ -1,0 +1,375 @@
+"""Benchmark of the fused attention forward on GB300 (one JSON line on stdout).
+
+A step is one call of the fused forward over one batch of the headline workload
+(B=2, H=32, N=4096, d=128, non-causal, bf16 inputs from the seeded generator), inputs resident
+in HBM.  ``value`` is whole-job TFLOPS (4*B*H*N^2*d per step, summed over ranks, over the max
+rank time).  Timing: W untimed warm-up steps, then K steps timed with CUDA events on the
+launching stream, an L2 flush (a 256 MiB write) before each step outside the events, barrier and
+synchronize on both sides.  Extra keys: ``e2e`` (the same metric through the public API with
+pinned host buffers and the host<->device copies inside the timed region), ``roofline`` (the
+kernel against the measured bf16 tensor peak), ``cpu_baseline`` (the float64 oracle on a bounded
+sample), ``unfused`` (the three-kernel comparison path) and ``clocks``.
+
+``--impl reference`` times the float64 CPU oracle (the only reference this method has) on the
+host cores instead, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gen import configs  # noqa: E402
+from io_aware_attention_attn_gb300 import accounting as acc  # noqa: E402
+
+METRIC = "fused attention fwd TFLOPS at d=128 N=4096; % of BF16 tensor peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def sources_digest() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "io_aware_attention_attn_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "_source": "fallback"}
+
+
+def profiled_traffic(kernel_tag: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(f).read()
+        m = re.search(r"traffic_bytes_per_launch\[" + re.escape(kernel_tag) +
+                      r"\]:\s*(\d+)\s+sources:\s*(\w+)", text)
+        if m and m.group(2) == sources_digest():
+            return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(1.0)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.out.flush()
+        rows = [r.split(", ") for r in open(self.out.name).read().strip().splitlines() if r]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_cores() -> int:
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        blas = [i["num_threads"] for i in info if i.get("user_api") == "blas"]
+        if blas:
+            return int(max(blas))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(w, q, k, v, target_s: float, max_rows: int | None = None):
+    """Time the float64 oracle on rows of head (0,0) until ~target_s seconds; TFLOPS + sample."""
+    from oracle import attention as orc
+    N = w.N
+    rows_done, flops, t_total = 0, 0.0, 0.0
+    step = 128
+    while t_total < target_s and rows_done < (max_rows or N * w.B * w.H):
+        r0 = rows_done % N
+        hidx = rows_done // N
+        b, h = divmod(hidx % (w.B * w.H), w.H)
+        rows = np.arange(r0, min(N, r0 + step))
+        t0 = time.perf_counter()
+        orc.attention_head_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
+        t_total += time.perf_counter() - t0
+        vis = [(int(r) + 1) if w.causal else N for r in rows]
+        flops += sum(4.0 * x * w.d for x in vis)
+        rows_done += len(rows)
+        step = min(step * 2, 1024)
+    return flops / t_total / 1e12, rows_done, t_total
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    q, k, v, _ = w.make()
+    cores = cpu_cores()
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, per_step)
+    vals, times, rows = [], [], 0
+    for _ in range(args.steps):
+        tf, r, t = oracle_sample(w, q, k, v, per_step)
+        vals.append(tf)
+        times.append(t)
+        rows += r
+    value = len(vals) / sum(1.0 / x for x in vals)  # flops-weighted mean of equal-time steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded splitmix64/Box-Muller, bf16-rounded)",
+        "config": {**w.describe(), "l2": "n/a (host)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"float64 oracle rows of head (0,0) of {w.name}: "
+                                   f"{rows} rows over {args.steps} steps"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, rank, world, dist):
+    import torch
+    from io_aware_attention_attn_gb300 import attn, build
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    attn.lib()
+    q_np, k_np, v_np, _ = w.make()
+
+    def to_dev(x):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = to_dev(q_np), to_dev(k_np), to_dev(v_np)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = acc.attention_flops(w.H, [w.N] * w.B, w.d, w.causal)
+
+    def step():
+        attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    barrier()
+    clock_info = clocks.stop()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms, one kernel launch each
+    total_ms = sum(per)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    if attn.last_device_error() != 0:
+        raise RuntimeError("device-side pipeline wait timed out during the bench")
+
+    peaks = measured_peaks()
+    kernel_ms = statistics.mean(per)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic("attn_fwd_kernel"),
+                "peak_source": f"{peaks['_source']} bf16 burst (cuBLAS)",
+                "algorithmic_bytes": acc.attention_ideal_bytes(w.H, w.B * w.N, w.d)}
+
+    # ---- end to end through the public API: pinned host -> device, forward, device -> host
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hk = torch.from_numpy(k_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hv = torch.from_numpy(v_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        n_e2e = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            dq = hq.to(dev, non_blocking=True)
+            dk = hk.to(dev, non_blocking=True)
+            dv = hv.to(dev, non_blocking=True)
+            oo, ll = attn.attn_fwd(dq, dk, dv, causal=w.causal, scale=w.scale)
+            ho.copy_(oo, non_blocking=True)
+            hl.copy_(ll, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": flops * n_e2e * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": 3 * q.numel() * 2,
+               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4, "steps": n_e2e}
+        del hq, hk, hv, ho, hl
+
+    # ---- unfused three-kernel comparison path (memory wall)
+    unfused = None
+    if not args.no_unfused:
+        try:
+            need = attn.unfused_workspace_bytes(w.B, w.H, w.N, w.d)
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            ou = torch.empty_like(o)
+            lu = torch.empty_like(lse)
+            for _ in range(2):
+                attn.attn_fwd_unfused(q, k, v, causal=w.causal, scale=w.scale, workspace=ws,
+                                      out=ou, lse=lu)
+            barrier()
+            n_u = 5
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(n_u):
+                attn.attn_fwd_unfused(q, k, v, causal=w.causal, scale=w.scale, workspace=ws,
+                                      out=ou, lse=lu)
+            u1.record(stream)
+            barrier()
+            u_ms = u0.elapsed_time(u1) / n_u
+            ub = acc.unfused_bytes(w.B, w.H, w.N, w.d)
+            unfused = {"ms_per_step": u_ms, "tflops": flops / (u_ms * 1e-3) / 1e12,
+                       "algorithmic_bytes": ub, "gbs": ub / (u_ms * 1e-3) / 1e9,
+                       "hbm_frac": ub / (u_ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                       "fused_speedup": u_ms / kernel_ms, "launches_per_step": 3}
+            del ws
+        except Exception as e:  # reported, never silently replaced
+            unfused = {"error": str(e)[:200]}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"float64 oracle, {rows} query rows of head (0,0) of {w.name}, "
+                         f"{secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded splitmix64/Box-Muller, bf16-rounded)",
+            "config": {**w.describe(), "l2": "flushed (256 MiB write) before every step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_bf16_peak": 100.0 * value / world / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "unfused": unfused,
+            "clocks": clock_info, "gpu_launches": args.steps,
+            "kernel_ms_median": statistics.median(per),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=configs.HEADLINE)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = configs.WORKLOADS[args.workload]
+    if w.varlen:
+        ap.error("the bench times dense workloads")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist_mod.init_process_group(backend)
+        dist = dist_mod
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+    else:
+        run_ours(args, w, rank, world, dist)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

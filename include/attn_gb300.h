@@ -1,0 +1,132 @@
+/*
+ * attn_gb300.h -- C ABI of the GB300 (sm_103a) IO-aware attention forward library.
+ *
+ * The operation is scaled dot-product attention, O = softmax(scale * Q K^T) V, computed row by
+ * row over the keys each query may see, together with the per-row log-sum-exp of the scaled
+ * scores (CS336 Lecture 5 notes, section 6.1 for the definition; section 6.2 for the fused,
+ * tiled, online-softmax forward that never writes the score matrix to HBM and keeps only m and l
+ * "merged into a logsumexp"; CS336 GPU/attention notes, "Online softmax 回顾", for the merge).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library allocates no
+ *     device memory (the fused kernel uses on-chip shared and tensor memory only; the unfused
+ *     comparison path uses a caller-provided workspace).
+ *   - Element types: q, k, v, o are bfloat16 (passed as void*); lse is float32;
+ *     cu_seqlens is int32.
+ *   - Dense layout (cu_seqlens == NULL): q, k, v, o are [B, H, N, d] contiguous, d innermost;
+ *     lse is [B, H, N].
+ *   - Packed variable-length layout (cu_seqlens != NULL): B is the number of sequences and N is
+ *     the total token count T = cu_seqlens[B] (passed by the host, which never reads device
+ *     memory); q, k, v, o are [H, T, d] and lse is [H, T].  Sequence s owns rows
+ *     cu_seqlens[s] .. cu_seqlens[s+1]-1 of every head and attends only to itself.
+ *     cu_seqlens must be non-decreasing with cu_seqlens[0] = 0 and cu_seqlens[B] = N; a
+ *     violation is the caller's error and gives undefined output (never an out-of-bounds write
+ *     outside [0, N) rows of o and lse).  Zero-length sequences are allowed and write nothing.
+ *   - causal != 0 keeps key j for query i iff j <= i, positions counted from the start of each
+ *     sequence.
+ *   - scale multiplies the scores before the softmax (1/sqrt(d) for the usual attention); it must
+ *     be finite and > 0.  lse is the natural-log log-sum-exp of the scaled scores.
+ *   - d must be 64 or 128.  Pointers must be 16-byte aligned.
+ *   - B, H, N >= 0; if any of them is 0 there is nothing to compute and the call returns
+ *     ATTN_OK without touching the pointers.
+ *   - Work is enqueued on `stream` (a cudaStream_t, 0 = legacy default stream) and runs
+ *     asynchronously.  The return value covers host-side validation and the launch; a device-side
+ *     failure (a pipeline wait that timed out) is reported by attn_get_last_device_error().
+ *   - On any non-zero return the contents of o and lse are unspecified.
+ *   - Entry points are thread-safe as long as concurrent calls use different output buffers.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = -1,        /* a required pointer is NULL                                  */
+  ATTN_ERR_HEAD_DIM = -2,    /* d is not 64 or 128                                          */
+  ATTN_ERR_SHAPE = -3,       /* a negative size, or sizes whose products overflow the kernel */
+  ATTN_ERR_ALIGN = -4,       /* a tensor pointer is not 16-byte aligned                     */
+  ATTN_ERR_LAUNCH = -5,      /* a CUDA call failed while preparing or launching the kernel  */
+  ATTN_ERR_DEVICE = -6,      /* the current device is not an sm_103 (GB300-class) GPU       */
+  ATTN_ERR_SCALE = -7,       /* scale is not finite or not > 0                              */
+  ATTN_ERR_WORKSPACE = -8,   /* workspace NULL, unaligned or smaller than required          */
+  ATTN_ERR_UNSUPPORTED = -9  /* an argument combination this entry point does not support   */
+} attn_status;
+
+/*
+ * Fused forward (the hot path).  One kernel launch: each CTA keeps a 128-row tile of Q on chip,
+ * streams 128-row tiles of K and V through TMA-fed shared memory, computes S = Q K^T with tcgen05
+ * tensor-core MMAs into tensor memory, applies the online softmax (running row max m and sum l,
+ * exp2 of log2(e)-prescaled scores, rescaling of the O accumulator) and accumulates P V on the
+ * tensor cores, then writes O = acc / l in bf16 and lse = m + ln l in fp32.  The N x N score
+ * matrix never reaches HBM; causal tiles above the diagonal are skipped.
+ *   q, k, v : bf16 inputs (read only)          o   : bf16 output, same layout as q
+ *   lse     : fp32 output                      cu_seqlens : NULL (dense) or int32[B+1] (packed)
+ *   B, H, N, d, causal, scale : as described above; stream : cudaStream_t
+ * Returns an attn_status.
+ */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             const int32_t* cu_seqlens, int B, int H, int N, int d, int causal, float scale,
+             void* stream);
+
+/*
+ * Unfused comparison path (the "standard attention" of the pages: S written to HBM, read back for
+ * the softmax, P written to HBM, read back for P V; CS336 GPU/attention notes, "Attention 为什么
+ * 容易 memory-bound"; CS336 Lecture 5 notes, section 6.1).  Three kernel launches on `stream`:
+ * scores (S = scale * Q K^T in fp32), row softmax (P in bf16 plus lse), and P V.  It computes the
+ * same O and lse as attn_fwd and exists only as the memory-wall comparison.
+ * Dense layout only (cu_seqlens must be NULL, else ATTN_ERR_UNSUPPORTED).
+ *   workspace : caller-owned device buffer of at least attn_fwd_unfused_workspace_bytes(B,H,N,d)
+ *               bytes, 256-byte aligned; its contents on return are unspecified.
+ */
+ATTN_API int attn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int32_t* cu_seqlens, int B, int H, int N, int d, int causal,
+                     float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes attn_fwd_unfused needs for a dense [B, H, N, d] problem: the fp32 score matrix
+ * and the bf16 (unnormalised) probability matrix of every head, each row padded to a multiple of
+ * 128 columns, plus one fp32 normaliser per row: about B * H * N * (6 * Npad + 4) bytes with
+ * Npad = N rounded up to 128 (each region rounded up to 256 bytes).  Returns 0 for invalid sizes.
+ */
+ATTN_API size_t attn_fwd_unfused_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Device-side status of the kernels launched on `stream` since the previous call: 0 if every
+ * pipeline wait completed; otherwise a code whose low byte is 1 (a wait exceeded its time limit,
+ * after which the kernel drained its in-flight copies, released its tensor memory and returned),
+ * bits 8..15 name the waiting role and bits 16..23 the wait site.  Synchronises `stream`, then
+ * clears the status.  Returns ATTN_ERR_LAUNCH (< 0) if the status cannot be read.
+ */
+ATTN_API int attn_get_last_device_error(void* stream);
+
+/*
+ * Diagnostic: one 128-row tensor-core product with the operand layouts and descriptors of the fused
+ * kernel, written to d as fp32 row-major.  Not part of the attention path; it isolates the
+ * tcgen05 operand encoding (CS336 Lecture 5 notes, section 6.2: the two matmuls of each tile pair).
+ *   mode 0: d[128 x 128] = a[128 x dim] * b[128 x dim]^T   (the S = Q K^T shape)
+ *   mode 1: d[128 x dim] = a[128 x 128] * b[128 x dim]     (the O += P V shape)
+ *   a, b : bf16 row-major device buffers (16-byte aligned); d : fp32 device buffer;
+ *   dim  : 64 or 128.  Asynchronous on `stream`; returns an attn_status.
+ */
+ATTN_API int attn_selftest_mma(const void* a, const void* b, float* d, int mode, int dim, void* stream);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,170 @@
+"""Thin Python binding of ``libattn_gb300.so`` (ctypes): argument marshalling only.
+
+Every step of the attention forward runs in the library's CUDA kernels; PyTorch only supplies
+device memory, streams and the output allocations.  There is no fallback: if the library is
+missing or the GPU is not an sm_103 part, calls raise.
+
+Layouts (same as the C ABI in ``include/attn_gb300.h``):
+  dense  q, k, v, o: [B, H, N, d] bf16 contiguous; lse [B, H, N] fp32
+  packed q, k, v, o: [H, T, d] bf16 contiguous + cu_seqlens int32 [n+1]; lse [H, T] fp32
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gb300.so")
+
+STATUS = {
+    0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_HEAD_DIM", -3: "ATTN_ERR_SHAPE",
+    -4: "ATTN_ERR_ALIGN", -5: "ATTN_ERR_LAUNCH", -6: "ATTN_ERR_DEVICE", -7: "ATTN_ERR_SCALE",
+    -8: "ATTN_ERR_WORKSPACE", -9: "ATTN_ERR_UNSUPPORTED",
+}
+
+# exported C symbols and their ctypes signatures (kept in step with include/attn_gb300.h)
+_P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_unfused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "attn_fwd_unfused_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "attn_get_last_device_error": (_I, [_P]),
+    "attn_selftest_mma": (_I, [_P, _P, _P, _I, _I, _P]),
+    "attn_version": (_I, []),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library once (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m io_aware_attention_attn_gb300.build`"
+                " (or __graft_entry__.build())")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = handle
+    return _lib
+
+
+def _check(name: str, rc: int):
+    if rc != 0:
+        raise AttnError(name, rc)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_inputs(q, k, v, cu_seqlens):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+        if t.shape != q.shape or t.device != q.device:
+            raise ValueError("q, k and v must have the same shape and device")
+    if cu_seqlens is None:
+        if q.dim() != 4:
+            raise ValueError("dense inputs are [B, H, N, d]")
+        B, H, N, d = q.shape
+    else:
+        if q.dim() != 3:
+            raise ValueError("packed inputs are [H, T, d] with cu_seqlens")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or \
+                not cu_seqlens.is_contiguous() or cu_seqlens.dim() != 1 or \
+                cu_seqlens.device != q.device:
+            raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor on q's device")
+        H, N, d = q.shape
+        B = cu_seqlens.numel() - 1
+    return B, H, N, d
+
+
+def attn_fwd(q, k, v, cu_seqlens=None, causal: bool = False, scale: float | None = None,
+             out=None, lse=None, stream=None):
+    """Fused attention forward.  Returns (O bf16 like q, LSE fp32)."""
+    import torch
+    B, H, N, d = _check_inputs(q, k, v, cu_seqlens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), cu_seqlens.data_ptr() if cu_seqlens is not None else None,
+                            B, H, N, d, int(bool(causal)), float(scale),
+                            _stream_handle(stream, q.device))
+    _check("attn_fwd", rc)
+    return out, lse
+
+
+def unfused_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().attn_fwd_unfused_workspace_bytes(B, H, N, d))
+
+
+def attn_fwd_unfused(q, k, v, causal: bool = False, scale: float | None = None, workspace=None,
+                     out=None, lse=None, stream=None):
+    """Unfused three-kernel comparison path (S and P through HBM).  Dense layout only."""
+    import torch
+    B, H, N, d = _check_inputs(q, k, v, None)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = unfused_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_unfused(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), None, B, H, N, d, int(bool(causal)),
+                                    float(scale), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream, q.device))
+    _check("attn_fwd_unfused", rc)
+    return out, lse
+
+
+def last_device_error(stream=None, device=None) -> int:
+    """Device status word of the kernels on ``stream`` (0 = every pipeline wait completed)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        rc = lib().attn_get_last_device_error(_stream_handle(stream, dev))
+    if rc < 0:
+        raise AttnError("attn_get_last_device_error", rc)
+    return rc
+
+
+def selftest_mma(a, b, mode: int):
+    """Diagnostic single-tile tensor-core product (see attn_selftest_mma in the header)."""
+    import torch
+    dim = b.shape[1]
+    n_out = 128 if mode == 0 else dim
+    d = torch.empty((128, n_out), dtype=torch.float32, device=a.device)
+    with torch.cuda.device(a.device):
+        rc = lib().attn_selftest_mma(a.data_ptr(), b.data_ptr(), d.data_ptr(), mode, dim,
+                                     _stream_handle(None, a.device))
+    _check("attn_selftest_mma", rc)
+    return d
+
+
+def version() -> int:
+    return int(lib().attn_version())

@@ -1,0 +1,212 @@
+// attn_abi.cu -- the extern "C" entry points of libattn_gb300: argument validation, TMA map
+// encoding and kernel launch.  The arithmetic lives entirely in the CUDA kernels.
+#include <atomic>
+#include <cmath>
+#include <climits>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "attn_gb300.h"
+#include "attn_host.h"
+#include "attn_params.h"
+
+namespace attn {
+
+__device__ int g_attn_status = 0;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_ok[kMaxDevices];          // 0 unknown, 1 sm_103, 2 other
+std::atomic<int*> g_status_ptr[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int encode_rows_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows,
+                    uint64_t heads) {
+  auto fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[3] = {d, rows, heads};
+  const cuuint64_t strides[2] = {d * 2, d * 2 * rows};  // bytes, dims 1 and 2
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int encode_f32_rows_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                        uint64_t heads) {
+  auto fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[3] = {cols, rows, heads};
+  const cuuint64_t strides[2] = {cols * 4, cols * 4 * rows};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+  int st = g_dev_ok[dev].load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    st = (major == 10 && minor == 3) ? 1 : 2;
+    g_dev_ok[dev].store(st, std::memory_order_release);
+  }
+  return st == 1 ? 0 : ATTN_ERR_DEVICE;
+}
+
+int* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_attn_status) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(addr);
+    g_status_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+// Shared validation of attn_fwd / attn_fwd_unfused.  Sets *empty when there is nothing to do.
+static int validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const int32_t* cu, int B, int H, int N, int d, float scale, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (cu != nullptr && B == 0 && N > 0) return ATTN_ERR_SHAPE;  // tokens but no sequences
+  if (B == 0 || H == 0 || N == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
+  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_ALIGN;
+  if (cu != nullptr && (reinterpret_cast<uintptr_t>(cu) & 3u)) return ATTN_ERR_ALIGN;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SCALE;
+  // grid sizes must fit the kernel's 32-bit indices
+  const long long tiles_per_head = (static_cast<long long>(N) + kBM - 1) / kBM;
+  const long long grid = cu ? (tiles_per_head + B) * H
+                            : tiles_per_head * static_cast<long long>(B) * H;
+  if (grid > INT_MAX) return ATTN_ERR_SHAPE;
+  if (cu == nullptr && static_cast<long long>(B) * H > INT_MAX) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens, int B, int H, int N, int d, int causal,
+                        float scale, void* stream) {
+  bool empty = false;
+  int rc = validate(q, k, v, o, lse, cu_seqlens, B, H, N, d, scale, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  if ((rc = check_device()) != 0) return rc;
+  FwdParams p{};
+  const bool varlen = cu_seqlens != nullptr;
+  const uint64_t heads = varlen ? static_cast<uint64_t>(H) : static_cast<uint64_t>(B) * H;
+  if (encode_rows_map(&p.tm_q, q, d, N, heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_k, k, d, N, heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_v, v, d, N, heads) != CUDA_SUCCESS)
+    return ATTN_ERR_LAUNCH;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.status = status_word();
+  if (!p.status) return ATTN_ERR_LAUNCH;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.n_qt = (N + kBM - 1) / kBM;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int grid = varlen ? (p.n_qt + B) * H : p.n_qt * B * H;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, grid, st)
+                                  : launch_fwd_d128(p, causal != 0, varlen, grid, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const int32_t* cu_seqlens, int B, int H, int N, int d, int causal,
+                                float scale, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (cu_seqlens != nullptr) return ATTN_ERR_UNSUPPORTED;
+  bool empty = false;
+  int rc = validate(q, k, v, o, lse, nullptr, B, H, N, d, scale, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  const size_t need = attn_fwd_unfused_workspace_bytes(B, H, N, d);
+  if (need == 0) return ATTN_ERR_SHAPE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  if ((rc = check_device()) != 0) return rc;
+  UnfusedArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.status = status_word();
+  if (!a.status) return ATTN_ERR_LAUNCH;
+  return launch_unfused(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                             : ATTN_ERR_LAUNCH;
+}
+
+extern "C" size_t attn_fwd_unfused_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  return unfused_workspace_layout(B, H, N).total;
+}
+
+extern "C" int attn_get_last_device_error(void* stream) {
+  int* addr = status_word();
+  if (!addr) return ATTN_ERR_LAUNCH;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int value = 0;
+  if (cudaMemcpyAsync(&value, addr, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if (value != 0) {
+    const int zero = 0;
+    if (cudaMemcpyAsync(addr, &zero, sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+  }
+  return value;
+}
+
+extern "C" int attn_version(void) { return 100; }

@@ -1,0 +1,98 @@
+"""The C-ABI library on the host: it builds, loads, exports what the header declares, and its
+argument validation returns the documented codes before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from io_aware_attention_attn_gb300 import attn, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "attn_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return attn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert set(names) == set(attn.SIGNATURES), names
+    for must in ("attn_fwd", "attn_fwd_unfused", "attn_fwd_unfused_workspace_bytes",
+                 "attn_get_last_device_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.attn_version() >= 100
+
+
+def test_only_the_api_is_exported(lib):
+    out = os.popen(f"nm -D --defined-only {attn.LIB_PATH}").read().split("\n")
+    exported = {l.split()[-1] for l in out if re.search(r" [TD] ", l)}
+    assert {n for n in exported if not n.startswith("_")} <= set(attn.SIGNATURES) | {"_init", "_fini"}
+
+
+ALIGNED = 0x10000  # fake, never dereferenced: validation fails before any CUDA call
+
+
+def call(lib, q=ALIGNED, k=ALIGNED, v=ALIGNED, o=ALIGNED, lse=ALIGNED, cu=None, B=1, H=1, N=128,
+         d=128, causal=0, scale=0.125):
+    return lib.attn_fwd(q, k, v, o, lse, cu, B, H, N, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), -3), (dict(H=-2), -3), (dict(N=-5), -3),
+    (dict(d=96), -2), (dict(d=256), -2), (dict(d=0), -2),
+    (dict(q=None), -1), (dict(lse=None), -1), (dict(o=None), -1),
+    (dict(k=ALIGNED + 8), -4), (dict(o=ALIGNED + 2), -4), (dict(lse=ALIGNED + 4), -4),
+    (dict(cu=ALIGNED + 2), -4),
+    (dict(scale=0.0), -7), (dict(scale=-1.0), -7), (dict(scale=float("inf")), -7),
+    (dict(scale=float("nan")), -7),
+    (dict(cu=ALIGNED, B=0, N=5), -3),
+    (dict(N=(1 << 31) - 1, B=1 << 10, H=1 << 10), -3),
+])
+def test_validation_codes(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(N=0), dict(N=0, q=None, o=None),
+                                dict(cu=ALIGNED, N=0, B=3)])
+def test_empty_problems_are_noops(lib, kw):
+    assert call(lib, **kw) == 0
+
+
+def test_unfused_workspace_bytes(lib):
+    assert lib.attn_fwd_unfused_workspace_bytes(2, 32, 4096, 128) == 64 * 4096 * (4096 * 6 + 4)
+    assert lib.attn_fwd_unfused_workspace_bytes(1, 1, 100, 64) == 51200 + 25600 + 512
+    assert lib.attn_fwd_unfused_workspace_bytes(1, 1, 100, 96) == 0
+    assert lib.attn_fwd_unfused_workspace_bytes(0, 1, 100, 64) == 0
+
+
+def test_unfused_validation(lib):
+    f = lib.attn_fwd_unfused
+    assert f(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, None, 1, 1, 128, 64, 0, 0.125,
+             None, 1 << 20, None) == -8
+    assert f(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, None, 1, 1, 128, 64, 0, 0.125,
+             ALIGNED, 100, None) == -8
+    assert f(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, None, 1, 1, 128, 64, 0, 0.125,
+             ALIGNED + 16, 1 << 20, None) == -8
+    assert f(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 1, 1, 128, 64, 0, 0.125,
+             ALIGNED, 1 << 20, None) == -9
+    assert f(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, None, 1, 1, 128, 80, 0, 0.125,
+             ALIGNED, 1 << 20, None) == -2
+
+
+def test_selftest_validation(lib):
+    assert lib.attn_selftest_mma(None, ALIGNED, ALIGNED, 0, 128, None) == -1
+    assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 0, 32, None) == -2
+    assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 7, 64, None) == -9
