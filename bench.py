@@ -40,10 +40,14 @@ METRIC = "fused attention fwd TFLOPS at d=128 N=4096; % of BF16 tensor peak"
 L2_FLUSH_BYTES = 256 << 20
 
 
+# the files that make up the fused kernel: a profile taken on other contents is stale
+FUSED_SOURCES = ("attn_fwd_kernel.cuh", "attn_params.h", "sm103_ptx.cuh", "attn_fwd_d128.cu")
+
+
 def sources_digest() -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "io_aware_attention_attn_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+    for f in FUSED_SOURCES:
+        h.update(open(os.path.join(ROOT, "io_aware_attention_attn_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -113,6 +117,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest of every rank's ``value`` (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def cpu_cores() -> int:
     try:
         import threadpoolctl
@@ -126,7 +140,8 @@ def cpu_cores() -> int:
 
 
 def oracle_sample(w, q, k, v, target_s: float, max_rows: int | None = None):
-    """Time the float64 oracle on rows of head (0,0) until ~target_s seconds; TFLOPS + sample."""
+    """Time the float64 oracle on query rows of the workload (head-major, from head (0, 0))
+    until about ``target_s`` seconds have passed; returns (TFLOPS, rows, seconds)."""
     from oracle import attention as orc
     N = w.N
     rows_done, flops, t_total = 0, 0.0, 0.0
@@ -169,8 +184,8 @@ def run_reference(args, w, rank, world):
         "config": {**w.describe(), "l2": "n/a (host)"},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                         "sample": f"float64 oracle rows of head (0,0) of {w.name}: "
-                                   f"{rows} rows over {args.steps} steps"},
+                         "sample": f"float64 oracle, {rows} query rows (head-major from head "
+                                   f"(0,0)) of {w.name} over {args.steps} steps"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -223,11 +238,7 @@ def run_ours(args, w, rank, world, dist):
     barrier()
     clock_info = clocks.stop()
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms, one kernel launch each
-    total_ms = sum(per)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per), dist, dev)
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     if attn.last_device_error() != 0:
         raise RuntimeError("device-side pipeline wait timed out during the bench")
@@ -269,11 +280,7 @@ def run_ours(args, w, rank, world, dist):
             e2e_step()
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
         e2e = {"value": flops * n_e2e * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "h2d_bytes_per_step": 3 * q.numel() * 2,
                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4, "steps": n_e2e}
@@ -314,8 +321,8 @@ def run_ours(args, w, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline:
         tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"float64 oracle, {rows} query rows of head (0,0) of {w.name}, "
-                         f"{secs:.1f} s"}
+               "sample": f"float64 oracle, {rows} query rows (head-major from head (0,0)) "
+                         f"of {w.name}, {secs:.1f} s"}
 
     if rank == 0:
         line = {

@@ -122,6 +122,15 @@ ATTN_API int attn_get_last_device_error(void* stream);
  */
 ATTN_API int attn_selftest_mma(const void* a, const void* b, float* d, int mode, int dim, void* stream);
 
+/*
+ * Diagnostic: launch one warp that waits on an mbarrier nothing ever arrives on, through the same
+ * bounded wait the pipeline kernels use.  After the wait limit (one second) the warp records
+ * status 1 | (6 << 8) | (1 << 16) and returns, leaving the context usable; read it with
+ * attn_get_last_device_error().  Exercises failure detection without faulting or hanging the GPU.
+ * Returns an attn_status (the launch only).
+ */
+ATTN_API int attn_selftest_wait_timeout(void* stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 ATTN_API int attn_version(void);
 

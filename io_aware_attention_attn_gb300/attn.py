@@ -30,6 +30,7 @@ SIGNATURES = {
     "attn_fwd_unfused_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_get_last_device_error": (_I, [_P]),
     "attn_selftest_mma": (_I, [_P, _P, _P, _I, _I, _P]),
+    "attn_selftest_wait_timeout": (_I, [_P]),
     "attn_version": (_I, []),
 }
 
@@ -164,6 +165,19 @@ def selftest_mma(a, b, mode: int):
                                      _stream_handle(None, a.device))
     _check("attn_selftest_mma", rc)
     return d
+
+
+def selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test (returns at once; the status appears after ~1 s)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check("attn_selftest_wait_timeout",
+           lib().attn_selftest_wait_timeout(_stream_handle(stream, dev)))
+
+
+def decode_status(code: int) -> dict:
+    """Split a device status word into kind, role and wait site."""
+    return {"kind": code & 0xFF, "role": (code >> 8) & 0xFF, "site": (code >> 16) & 0xFF}
 
 
 def version() -> int:

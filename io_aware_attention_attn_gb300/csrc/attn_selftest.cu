@@ -125,3 +125,34 @@ extern "C" int attn_selftest_mma(const void* a, const void* b, float* d, int mod
   mma_selftest_kernel<<<1, 128, kSelftestSmem, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
+
+// ------------------------------------------------------------------ bounded-wait self-test
+namespace attn {
+namespace {
+
+__global__ void wait_timeout_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);  // nobody ever arrives
+    fence_barrier_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  const WaitCtx wc{&abort_flag, status};
+  mbar_wait_warp(b, 0, wc, 6, 1);  // gives up after kWaitLimitNs and records the status
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_selftest_wait_timeout(void* stream) {
+  using namespace attn;
+  int rc = check_device();
+  if (rc != 0) return rc;
+  int* status = status_word();
+  if (!status) return ATTN_ERR_LAUNCH;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
