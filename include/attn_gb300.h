@@ -61,7 +61,8 @@ typedef enum {
   ATTN_ERR_DEVICE = -6,      /* the current device is not an sm_103 (GB300-class) GPU       */
   ATTN_ERR_SCALE = -7,       /* scale is not finite or not > 0                              */
   ATTN_ERR_WORKSPACE = -8,   /* workspace NULL, unaligned or smaller than required          */
-  ATTN_ERR_UNSUPPORTED = -9  /* an argument combination this entry point does not support   */
+  ATTN_ERR_UNSUPPORTED = -9, /* an argument combination this entry point does not support   */
+  ATTN_ERR_SCRATCH_LIMIT = -10 /* the problem needs more than the built-in scratch (no-alloc) */
 } attn_status;
 
 /*
@@ -101,6 +102,28 @@ ATTN_API int attn_fwd_unfused(const void* q, const void* k, const void* v, void*
  * Npad = N rounded up to 128 (each region rounded up to 256 bytes).  Returns 0 for invalid sizes.
  */
 ATTN_API size_t attn_fwd_unfused_workspace_bytes(int B, int H, int N, int d);
+
+/* Size of the built-in scratch array of attn_fwd_unfused_noalloc (64 MiB per GPU). */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * The unfused comparison path without a workspace argument, for callers that cannot allocate
+ * device memory.  (The reference pages have no counterpart: this is a property of this library's
+ * interface, not of the method.)  Some callers cannot call cudaMalloc -- code running under a
+ * memory manager that owns every device allocation, or a runtime that forbids allocation once it
+ * has started -- so this entry point allocates nothing: its scratch is a file-scope device array of
+ * ATTN_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until the process exits.
+ *   Arguments as attn_fwd_unfused (dense layout only), without cu_seqlens and the workspace.
+ *   Returns ATTN_ERR_SCRATCH_LIMIT when attn_fwd_unfused_workspace_bytes(B, H, N, d) exceeds
+ *   ATTN_NOALLOC_SCRATCH_BYTES, before touching the GPU.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
+ *   device current); make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents (nothing in it needs to start
+ *   at zero); calls whose work overlaps on the GPU, e.g. on two streams, race on it.
+ */
+ATTN_API int attn_fwd_unfused_noalloc(const void* q, const void* k, const void* v, void* o,
+                                      float* lse, int B, int H, int N, int d, int causal,
+                                      float scale, void* stream);
 
 /*
  * Device-side status of the kernels launched on `stream` since the previous call: 0 if every

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gb3
 STATUS = {
     0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_HEAD_DIM", -3: "ATTN_ERR_SHAPE",
     -4: "ATTN_ERR_ALIGN", -5: "ATTN_ERR_LAUNCH", -6: "ATTN_ERR_DEVICE", -7: "ATTN_ERR_SCALE",
-    -8: "ATTN_ERR_WORKSPACE", -9: "ATTN_ERR_UNSUPPORTED",
+    -8: "ATTN_ERR_WORKSPACE", -9: "ATTN_ERR_UNSUPPORTED", -10: "ATTN_ERR_SCRATCH_LIMIT",
 }
 
 # exported C symbols and their ctypes signatures (kept in step with include/attn_gb300.h)
@@ -28,6 +28,7 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_unfused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_fwd_unfused_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "attn_fwd_unfused_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_get_last_device_error": (_I, [_P]),
     "attn_selftest_mma": (_I, [_P, _P, _P, _I, _I, _P]),
     "attn_selftest_wait_timeout": (_I, [_P]),
@@ -140,6 +141,27 @@ def attn_fwd_unfused(q, k, v, causal: bool = False, scale: float | None = None, 
                                     workspace.numel() * workspace.element_size(),
                                     _stream_handle(stream, q.device))
     _check("attn_fwd_unfused", rc)
+    return out, lse
+
+
+def attn_fwd_unfused_noalloc(q, k, v, causal: bool = False, scale: float | None = None,
+                             out=None, lse=None, stream=None):
+    """The unfused path using the library's built-in scratch instead of a workspace (for callers
+    that cannot allocate device memory; outputs may still be allocated here when not given)."""
+    import torch
+    B, H, N, d = _check_inputs(q, k, v, None)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_unfused_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                                            int(bool(causal)), float(scale),
+                                            _stream_handle(stream, q.device))
+    _check("attn_fwd_unfused_noalloc", rc)
     return out, lse
 
 
