@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 256 << 20
 
 
 # the files that make up the fused kernel: a profile taken on other contents is stale
-FUSED_SOURCES = ("attn_fwd_kernel.cuh", "attn_params.h", "sm103_ptx.cuh", "attn_fwd_d128.cu")
+FUSED_SOURCES = ("attn_fwd_pair_kernel.cuh", "attn_params.h", "sm103_ptx.cuh", "attn_fwd_d128.cu")
 
 
 def sources_digest() -> str:

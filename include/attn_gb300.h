@@ -140,6 +140,7 @@ ATTN_API int attn_get_last_device_error(void* stream);
  * tcgen05 operand encoding (CS336 Lecture 5 notes, section 6.2: the two matmuls of each tile pair).
  *   mode 0: d[128 x 128] = a[128 x dim] * b[128 x dim]^T   (the S = Q K^T shape)
  *   mode 1: d[128 x dim] = a[128 x 128] * b[128 x dim]     (the O += P V shape)
+ *   mode 2: as mode 1 with a staged in tensor memory (the P V shape with P kept on chip)
  *   a, b : bf16 row-major device buffers (16-byte aligned); d : fp32 device buffer;
  *   dim  : 64 or 128.  Asynchronous on `stream`; returns an attn_status.
  */

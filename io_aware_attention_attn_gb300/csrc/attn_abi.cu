@@ -146,7 +146,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.B = B;
   p.H = H;
   p.N = N;
-  p.n_qt = (N + kBM - 1) / kBM;
+  p.n_qt = (N + 2 * kBM - 1) / (2 * kBM);  // pairs of 128-row query tiles per head
   p.scale_log2 = scale * 1.4426950408889634f;
   const int grid = varlen ? (p.n_qt + B) * H : p.n_qt * B * H;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

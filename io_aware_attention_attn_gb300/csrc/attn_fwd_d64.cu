@@ -1,15 +1,15 @@
 // attn_fwd_d64.cu -- instantiations and launcher of the fused forward kernel for head dim 64.
 #include <atomic>
 
-#include "attn_fwd_kernel.cuh"
+#include "attn_fwd_pair_kernel.cuh"
 
 namespace attn {
 namespace {
 
 template <bool CAUSAL, bool VARLEN>
 cudaError_t launch(const FwdParams& p, int grid, cudaStream_t stream) {
-  auto* kernel = attn_fwd_kernel<64, CAUSAL, VARLEN>;
-  constexpr int kSmem = FwdLayout<64>::kDynBytes;
+  auto* kernel = attn_fwd_pair_kernel<64, CAUSAL, VARLEN>;
+  constexpr int kSmem = PairLayout<64>::kDynBytes;
   // the opt-in for more than 48 KB of dynamic shared memory is per device; remember it
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
@@ -21,7 +21,7 @@ cudaError_t launch(const FwdParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kernel<<<grid, kFwdThreads, kSmem, stream>>>(p);
+  kernel<<<grid, kPairThreads, kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

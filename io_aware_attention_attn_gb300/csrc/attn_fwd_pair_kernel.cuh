@@ -1,0 +1,450 @@
+// attn_fwd_pair_kernel.cuh -- fused IO-aware attention forward for sm_103a (GB300), two query
+// tiles per CTA.
+//
+// One CTA owns two adjacent 128-row query tiles (t = 0, 1) of one (sequence, head).  Both tiles
+// share every K and V tile the TMA producer streams through shared memory, so K/V traffic per
+// FLOP is half that of one tile per CTA.  The score matrix never leaves the chip: the tiled loop
+// and online softmax of the FlashAttention forward (CS336 Lecture 5 notes, section 6.2; the block
+// merge of the CS336 GPU/attention notes, "Online softmax 回顾").
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer: Q0 and Q1 once, then K_j and V_j into two-stage rings
+//   warp 1      MMA issuer (lane 0) and TMEM owner.  Per key tile j and query tile t:
+//               S_t = Q_t K_j^T into tensor memory, then O_t += P_t V_j with P_t read from tensor
+//               memory (the A operand of the MMA) and V_j from shared memory
+//   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1: one query row per thread (the
+//               TMEM lane its warp may access).  The two warpgroups work on different tiles at
+//               once, so one tile's softmax overlaps the other tile's MMAs.
+//
+// Tensor memory (512 columns): S_0 at 0, S_1 at 128 (fp32 128 x 128), O_0 at 256, O_1 at 256 + D.
+// P_t (bf16, two per column) overwrites the first 64 columns of S_t once the softmax has read S_t.
+// The next S_t product rewrites those columns, so the MMA warp waits for the P_t V product to
+// complete (a commit barrier) before issuing it: tcgen05 MMAs with different accumulators are not
+// ordered with respect to each other.
+//
+// Softmax in the exp2 domain: t = s * scale * log2(e), p = 2^(t - m).  The reference maximum m
+// moves only when a tile raises the row maximum by more than kTau (log2 units); O and l always
+// share the reference, so O / l is unchanged (the correction factor is applied exactly when the
+// reference moves).  O is divided by the sum of the bf16-rounded P (the weights the tensor cores
+// used); lse uses the sum of the unrounded values.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_params.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <int D, bool CAUSAL, bool VARLEN>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    attn_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
+  using Lay = PairLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_s);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);
+  const WaitCtx wc{reinterpret_cast<volatile int*>(misc + 1), p.status};
+  auto bar = [&](int i) -> uint32_t { return sbase + Lay::kBar + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Lay::bQ), 1);
+    for (int s = 0; s < kPairStagesK; ++s) {
+      mbar_init(bar(Lay::bKF + s), 1);
+      mbar_init(bar(Lay::bKE + s), 1);
+    }
+    for (int s = 0; s < kPairStagesV; ++s) {
+      mbar_init(bar(Lay::bVF + s), 1);
+      mbar_init(bar(Lay::bVE + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(Lay::bSF + t), 1);
+      mbar_init(bar(Lay::bPF + t), 4 * 32);
+      mbar_init(bar(Lay::bPV + t), 1);
+      mbar_init(bar(Lay::bOD + t), 1);
+    }
+    mbar_init(bar(Lay::bDR), 1);
+    fence_barrier_init();
+    misc[1] = 0;
+  }
+
+  // ---- which pair of query tiles this CTA owns: z = head slice of the tensor maps, y0 = first row
+  // of the sequence along the maps' row axis, pt = pair index within the sequence
+  int z, y0, seq_len, pt;
+  if constexpr (!VARLEN) {
+    const int BH = p.B * p.H;
+    const int L = blockIdx.x;
+    if constexpr (CAUSAL) {  // heaviest pairs (most key tiles) first
+      pt = p.n_qt - 1 - L / BH;
+      z = L % BH;
+    } else {                 // all pairs of a head together: its K and V stay in L2
+      z = L / p.n_qt;
+      pt = L % p.n_qt;
+    }
+    y0 = 0;
+    seq_len = p.N;
+  } else {
+    if (warp == 0) {
+      // slot -> (sequence, pair) by a warp-wide scan of the per-sequence pair counts; entries of
+      // cu_seqlens are clamped to [0, N] so no access leaves the buffers
+      int remaining = blockIdx.x / p.H;
+      int f_start = 0, f_len = 0, f_pt = -1;
+      for (int base = 0; base < p.B; base += 32) {
+        const int s = base + lane;
+        int start = 0, len = 0;
+        if (s < p.B) {
+          int a = __ldg(p.cu_seqlens + s), b = __ldg(p.cu_seqlens + s + 1);
+          a = min(max(a, 0), p.N);
+          b = min(max(b, a), p.N);
+          start = a;
+          len = b - a;
+        }
+        const int nt = (len + 2 * kBM - 1) / (2 * kBM);
+        int incl = nt;
+        #pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        const int excl = incl - nt;
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (remaining < total) {
+          const unsigned hit = __ballot_sync(0xffffffffu, remaining >= excl && remaining < incl);
+          const int src = hit ? __ffs(hit) - 1 : 0;
+          const int pair = remaining - __shfl_sync(0xffffffffu, excl, src);
+          f_start = __shfl_sync(0xffffffffu, start, src);
+          f_len = __shfl_sync(0xffffffffu, len, src);
+          f_pt = hit ? pair : -1;
+          break;
+        }
+        remaining -= total;
+      }
+      if (lane == 0) {
+        misc[2] = static_cast<uint32_t>(f_start);
+        misc[3] = static_cast<uint32_t>(f_len);
+        misc[4] = static_cast<uint32_t>(f_pt);
+      }
+    }
+  }
+  __syncthreads();
+  if constexpr (VARLEN) {
+    y0 = static_cast<int>(misc[2]);
+    seq_len = static_cast<int>(misc[3]);
+    pt = static_cast<int>(misc[4]);
+    z = blockIdx.x % p.H;
+    if (pt < 0) return;  // slot beyond the last pair of the batch (uniform for the CTA)
+  }
+
+  if (warp == 1) {
+    tmem_alloc(sbase + Lay::kMisc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  constexpr uint32_t kColS[2] = {0, 128};
+  constexpr uint32_t kColO[2] = {256, 256 + D};
+
+  // key tiles each query tile visits (0 if the tile starts past the end of the sequence)
+  const int n_keytiles = (seq_len + kBN - 1) / kBN;
+  int n_kv[2];
+  #pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = 2 * pt + t;
+    n_kv[t] = (qt * kBM >= seq_len) ? 0 : (CAUSAL ? qt + 1 : n_keytiles);
+  }
+  const int n_max = n_kv[0] > n_kv[1] ? n_kv[0] : n_kv[1];
+
+  if (warp == 0) {
+    // ===================================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      const uint64_t keep = l2_policy_evict_last();   // K/V are re-read by every query pair
+      const uint64_t once = l2_policy_evict_first();  // Q is read once
+      mbar_arrive_expect_tx(bar(Lay::bQ), 2 * Lay::kTile);
+      #pragma unroll
+      for (int t = 0; t < 2; ++t)
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sbase + Lay::kQ + t * Lay::kTile + c * 16384, &p.tm_q, bar(Lay::bQ),
+                           c * 64, y0 + (2 * pt + t) * kBM, z, once);
+      int nk = 0, nv = 0;
+      bool ok = true;
+      for (int j = 0; j < n_max; ++j) {
+        const int sk = j % kPairStagesK, sv = j % kPairStagesV;
+        if (j >= kPairStagesK &&
+            !(ok = mbar_wait(bar(Lay::bKE + sk),
+                             (static_cast<uint32_t>(j / kPairStagesK) & 1u) ^ 1u, wc, 0, 1)))
+          break;
+        mbar_arrive_expect_tx(bar(Lay::bKF + sk), Lay::kTile);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sbase + Lay::kK + sk * Lay::kTile + c * 16384, &p.tm_k,
+                           bar(Lay::bKF + sk), c * 64, y0 + j * kBN, z, keep);
+        ++nk;
+        if (j >= kPairStagesV &&
+            !(ok = mbar_wait(bar(Lay::bVE + sv),
+                             (static_cast<uint32_t>(j / kPairStagesV) & 1u) ^ 1u, wc, 0, 2)))
+          break;
+        mbar_arrive_expect_tx(bar(Lay::bVF + sv), Lay::kTile);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sbase + Lay::kV + sv * Lay::kTile + c * 16384, &p.tm_v,
+                           bar(Lay::bVF + sv), c * 64, y0 + j * kBN, z, keep);
+        ++nv;
+      }
+      if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
+        mbar_wait_drain(bar(Lay::bQ), 0);
+        for (int j = (nk > kPairStagesK ? nk - kPairStagesK : 0); j < nk; ++j)
+          mbar_wait_drain(bar(Lay::bKF + j % kPairStagesK),
+                          static_cast<uint32_t>(j / kPairStagesK) & 1u);
+        for (int j = (nv > kPairStagesV ? nv - kPairStagesV : 0); j < nv; ++j)
+          mbar_wait_drain(bar(Lay::bVF + j % kPairStagesV),
+                          static_cast<uint32_t>(j / kPairStagesV) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ===================================================================== MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
+    constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, false, true);     // P (TMEM), V MN-major
+    auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T (lane 0 only)
+      const uint32_t kbase = sbase + Lay::kK + (j % kPairStagesK) * Lay::kTile;
+      const uint32_t qbase = sbase + Lay::kQ + t * Lay::kTile;
+      #pragma unroll
+      for (int k = 0; k < D / 16; ++k) {  // K = 16 per instruction; 4 steps per 128-byte row
+        const uint32_t off = static_cast<uint32_t>((k >> 2) * 16384 + (k & 3) * 32);
+        mma_bf16_ss(tmem + kColS[t], sdesc_sw128(qbase + off, 16, 1024),
+                    sdesc_sw128(kbase + off, 16, 1024), kIdS, k > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(Lay::bSF + t));
+    };
+    auto wait_k = [&](int j) {
+      return mbar_wait_warp(bar(Lay::bKF + j % kPairStagesK),
+                            static_cast<uint32_t>(j / kPairStagesK) & 1u, wc, 1, 3);
+    };
+    bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 4) && wait_k(0);
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0, 0);
+        if (n_kv[1] > 0) issue_s(1, 0);
+        mma_commit(bar(Lay::bKE + 0));
+      }
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_max; ++j) {
+      const int sv = j % kPairStagesV;
+      bool v_ready = false;
+      #pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (j >= n_kv[t]) continue;
+        if (!(ok = mbar_wait_warp(bar(Lay::bPF + t), static_cast<uint32_t>(j) & 1u, wc, 1, 5)))
+          break;
+        if (!v_ready) {
+          if (!(ok = mbar_wait_warp(bar(Lay::bVF + sv),
+                                    static_cast<uint32_t>(j / kPairStagesV) & 1u, wc, 1, 6)))
+            break;
+          v_ready = true;
+          if constexpr (VARLEN) {
+            // rows of the last V tile past the end of the sequence belong to the next sequence:
+            // zero them so that P = 0 there cannot meet a non-finite value
+            const int valid = seq_len - j * kBN;
+            if (valid < kBN) {
+              const uint32_t vbase = sbase + Lay::kV + sv * Lay::kTile;
+              #pragma unroll
+              for (int c = 0; c < D / 64; ++c)
+                for (int i = valid * 8 + lane; i < kBN * 8; i += 32)
+                  st_shared_v4(vbase + c * 16384 + i * 16, 0u, 0u, 0u, 0u);
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+          }
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vbase = sbase + Lay::kV + sv * Lay::kTile;
+          #pragma unroll
+          for (int k = 0; k < kBN / 16; ++k)
+            mma_bf16_ts(tmem + kColO[t], tmem + kColS[t] + k * 8,
+                        sdesc_sw128(vbase + k * 2048, 16384, 1024), kIdO,
+                        (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(bar(Lay::bPV + t));
+          if (j == n_kv[t] - 1) mma_commit(bar(Lay::bOD + t));
+        }
+        __syncwarp();
+        if (j + 1 < n_kv[t]) {
+          // S_t for the next key tile rewrites the columns P_t was read from: wait for P_t V_j
+          if (!(ok = wait_k(j + 1))) break;
+          if (!(ok = mbar_wait_warp(bar(Lay::bPV + t), static_cast<uint32_t>(j) & 1u, wc, 1, 7)))
+            break;
+          tc_fence_after();
+          if (lane == 0) issue_s(t, j + 1);
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(bar(Lay::bVE + sv));
+        if (j + 1 < n_max) mma_commit(bar(Lay::bKE + (j + 1) % kPairStagesK));
+      }
+      __syncwarp();
+    }
+    if (!ok) {  // unwinding: wait for every MMA already issued
+      if (lane == 0) mma_commit(bar(Lay::bDR));
+      __syncwarp();
+      mbar_wait_drain(bar(Lay::bDR), 0);
+    }
+  } else {
+    // ===================================================================== softmax
+    const int t = (warp - 2) >> 2;     // query tile of this warpgroup
+    const int quarter = warp & 3;      // TMEM lanes this warp may access: 32*quarter .. +31
+    const int r = quarter * 32 + lane; // row of the tile = TMEM lane
+    const int qt = 2 * pt + t;
+    const int row = qt * kBM + r;      // row within the sequence
+    const int n = n_kv[t];
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t s_col = t_lane + kColS[t];
+    const uint32_t o_col = t_lane + kColO[t];
+    const float sl2 = p.scale_log2;
+    float m2 = -INFINITY;            // reference max of the scaled scores (log2 units)
+    float le[4] = {0.f, 0.f, 0.f, 0.f};  // sums of 2^(t - m), fp32
+    float lr[4] = {0.f, 0.f, 0.f, 0.f};  // the same values after rounding to bf16
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = mbar_wait_warp(bar(Lay::bSF + t), static_cast<uint32_t>(j) & 1u, wc, 2, 8)))
+        break;
+      tc_fence_after();
+      uint32_t u0[32], u1[32], u2[32], u3[32];
+      tmem_ld32(s_col + 0, u0);
+      tmem_ld32(s_col + 32, u1);
+      tmem_ld32(s_col + 64, u2);
+      tmem_ld32(s_col + 96, u3);
+      tmem_wait_ld_regs(u0);
+      tmem_wait_ld_regs(u1);
+      tmem_wait_ld_regs(u2);
+      tmem_wait_ld_regs(u3);
+      float s[128];
+      #pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s[i] = u2f(u0[i]);
+        s[32 + i] = u2f(u1[i]);
+        s[64 + i] = u2f(u2[i]);
+        s[96 + i] = u2f(u3[i]);
+      }
+      const int key0 = j * kBN;
+      if ((CAUSAL && j == qt) || key0 + kBN > seq_len) {
+        const int lim = CAUSAL ? min(seq_len - key0, row - key0 + 1) : (seq_len - key0);
+        #pragma unroll
+        for (int c = 0; c < kBN; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+      }
+      float mx[8];
+      #pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = s[k];
+      #pragma unroll
+      for (int c = 8; c < kBN; c += 16)
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[c + k], s[c + 8 + k]);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7])) * sl2;
+      const float m_new = (mt > m2 + kTau) ? mt : m2;
+      const bool moved = (m_new != m2);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = moved ? ex2_approx(m2 - m_use) : 1.f;
+      m2 = m_new;
+      if (moved) {
+        #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          le[k] *= alpha;
+          lr[k] *= alpha;
+        }
+      }
+
+      // P = 2^(t - m) in bf16, two per 32-bit word, over the first 64 columns of S_t; written in
+      // two halves so each half's words are dead once stored
+      const float neg_m = -m_use;
+      #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+        #pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 64 * h + 2 * i;
+          float x0, x1;
+          ffma2(x0, x1, s[c], s[c + 1], sl2, sl2, neg_m, neg_m);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          pk[i] = pack_bf16x2(p0, p1);
+          fadd2(le[2 * (i & 1)], le[2 * (i & 1) + 1], p0, p1);
+          add_bf16x2_f32(lr[2 * (i & 1)], lr[2 * (i & 1) + 1], pk[i]);
+        }
+        tmem_st32(s_col + 32 * h, pk);
+      }
+
+      // O_t holds P_t V up to key tile j-1 (that product completed before S_t was rewritten);
+      // bring it to the new reference max before P_t V_j is added
+      if (j > 0 && __any_sync(0xffffffffu, moved)) {
+        #pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_col + c * 32, o);
+          tmem_wait_ld_regs(o);
+          #pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+          tmem_st32(o_col + c * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(Lay::bPF + t));
+    }
+    if (n > 0 && ok) ok = mbar_wait_warp(bar(Lay::bOD + t), 0, wc, 2, 9);
+    if (n > 0 && ok) {
+      tc_fence_after();
+      const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
+      const float l_round = (lr[0] + lr[1]) + (lr[2] + lr[3]);
+      const bool valid = row < seq_len;
+      const float inv_l = 1.f / l_round;
+      const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
+                          static_cast<size_t>(y0) + static_cast<size_t>(row);
+      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);
+      #pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_col + c * 32, o);
+        tmem_wait_ld_regs(o);
+        uint32_t pk[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+        if (valid) {
+          #pragma unroll
+          for (int q = 0; q < 4; ++q)
+            orow[c * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn

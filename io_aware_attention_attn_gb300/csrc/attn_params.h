@@ -12,8 +12,6 @@ namespace attn {
 
 constexpr int kBM = 128;           // query rows per tile
 constexpr int kBN = 128;           // keys per tile
-constexpr int kStages = 2;         // depth of the K and V rings
-constexpr int kFwdThreads = 192;   // 6 warps: producer, MMA, 4 x softmax
 constexpr float kTau = 8.0f;       // tolerated growth of the row max before O is rescaled (log2)
 
 struct FwdParams {
@@ -25,37 +23,41 @@ struct FwdParams {
   const int* cu_seqlens;     // packed layout only
   int* status;               // device status word (bounded-wait failures)
   int B, H, N;               // N: sequence length (dense) or total tokens T (packed)
-  int n_qt;                  // dense: query tiles per head
+  int n_qt;                  // dense: query-tile pairs (256 rows) per head
   float scale_log2;          // scale * log2(e)
 };
 
+// ------------------------------------------------------- fused kernel: two query tiles per CTA
+constexpr int kPairThreads = 320;  // 10 warps: producer, MMA, 2 x 4 softmax
+constexpr int kPairStagesK = 2;    // K ring depth
+constexpr int kPairStagesV = 2;    // V ring depth
+
 template <int D>
-struct FwdLayout {
-  static constexpr int kTile = kBM * D * 2;     // one 128-row x D bf16 tile (D/64 blocks of 16 KB)
-  static constexpr int kPTile = kBM * kBN * 2;  // one 128 x 128 bf16 probability tile
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
-  static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kP = kV + kStages * kTile;
-  static constexpr int kBar = kP + 2 * kPTile;
+struct PairLayout {
+  static constexpr int kTile = kBM * D * 2;  // one 128-row x D bf16 tile (D/64 blocks of 16 KB)
+  static constexpr int kQ = 0;               // Q_0, Q_1
+  static constexpr int kK = kQ + 2 * kTile;
+  static constexpr int kV = kK + kPairStagesK * kTile;
+  static constexpr int kBar = kV + kPairStagesV * kTile;
   enum {
-    bQ = 0,                 // Q landed
-    bKF = 1,                // K stage full  [kStages]
-    bKE = bKF + kStages,    // K stage free  [kStages]
-    bVF = bKE + kStages,    // V stage full  [kStages]
-    bVE = bVF + kStages,    // V stage free  [kStages]
-    bSF = bVE + kStages,    // S buffer written by the MMA  [2]
-    bPF = bSF + 2,          // P_j written and O corrected (128 softmax threads arrive)
-    bOD = bPF + 1,          // P_j V_j accumulated
-    bDR = bOD + 1,          // drain after an abort
+    bQ = 0,                      // Q_0 and Q_1 landed
+    bKF = 1,                     // K stage full  [kPairStagesK]
+    bKE = bKF + kPairStagesK,    // K stage free  [kPairStagesK]
+    bVF = bKE + kPairStagesK,    // V stage full  [kPairStagesV]
+    bVE = bVF + kPairStagesV,    // V stage free  [kPairStagesV]
+    bSF = bVE + kPairStagesV,    // S_t written                [2]
+    bPF = bSF + 2,               // P_t written, O_t corrected [2] (128 arrivals)
+    bPV = bPF + 2,               // P_t V_j completed          [2]
+    bOD = bPV + 2,               // last P_t V completed       [2]
+    bDR = bOD + 2,               // drain after an abort
     kNumBars = bDR + 1
   };
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..4] tile info
   static constexpr int kBytes = kMisc + 32;
-  static constexpr int kDynBytes = kBytes + 1024;    // slack to align the base to 1024 bytes
+  static constexpr int kDynBytes = kBytes + 1024;
 };
 
-static_assert(FwdLayout<128>::kDynBytes <= 232448, "fused kernel exceeds 227 KB shared memory");
+static_assert(PairLayout<128>::kDynBytes <= 232448, "pair kernel exceeds 227 KB shared memory");
 
 // Host launchers (one translation unit per head dimension).
 cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, bool varlen, int grid,

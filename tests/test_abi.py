@@ -96,3 +96,4 @@ def test_selftest_validation(lib):
     assert lib.attn_selftest_mma(None, ALIGNED, ALIGNED, 0, 128, None) == -1
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 0, 32, None) == -2
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 7, 64, None) == -9
+    assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, -1, 64, None) == -9

@@ -18,7 +18,7 @@ def _gpu():
 
 
 @pytest.mark.parametrize("dim", [64, 128])
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_single_tile_product(mode, dim):
     g = torch.Generator().manual_seed(7 + dim + mode)
     a_cols = dim if mode == 0 else 128
