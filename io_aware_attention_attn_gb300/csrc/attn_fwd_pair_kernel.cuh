@@ -222,14 +222,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // ===================================================================== MMA issuer
     constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
     constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, false, true);     // P (TMEM), V MN-major
+    // Operand descriptors are built once; every MMA adds a compile-time offset to the 14-bit
+    // start-address field (shared addresses stay below 256 KB, so the add never carries out of
+    // it).  Recomputing them per instruction made the single issuing thread, not the tensor pipe,
+    // the bottleneck.
+    constexpr uint64_t kTileD = static_cast<uint64_t>(Lay::kTile >> 4);
+    const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);
+    const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
+    const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16384, 1024);
     auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T (lane 0 only)
-      const uint32_t kbase = sbase + Lay::kK + (j % kPairStagesK) * Lay::kTile;
-      const uint32_t qbase = sbase + Lay::kQ + t * Lay::kTile;
+      const uint64_t a = desc_q + static_cast<uint64_t>(t) * kTileD;
+      const uint64_t b = desc_k + static_cast<uint64_t>(j % kPairStagesK) * kTileD;
+      const uint32_t d = tmem + kColS[t];
       #pragma unroll
       for (int k = 0; k < D / 16; ++k) {  // K = 16 per instruction; 4 steps per 128-byte row
-        const uint32_t off = static_cast<uint32_t>((k >> 2) * 16384 + (k & 3) * 32);
-        mma_bf16_ss(tmem + kColS[t], sdesc_sw128(qbase + off, 16, 1024),
-                    sdesc_sw128(kbase + off, 16, 1024), kIdS, k > 0 ? 1u : 0u);
+        const uint64_t off = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+        mma_bf16_ss(d, a + off, b + off, kIdS, k > 0 ? 1u : 0u);
       }
       mma_commit(bar(Lay::bSF + t));
     };
@@ -277,11 +285,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t vbase = sbase + Lay::kV + sv * Lay::kTile;
+          const uint64_t b = desc_v + static_cast<uint64_t>(sv) * kTileD;
+          const uint32_t d = tmem + kColO[t], a = tmem + kColS[t];
           #pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            mma_bf16_ts(tmem + kColO[t], tmem + kColS[t] + k * 8,
-                        sdesc_sw128(vbase + k * 2048, 16384, 1024), kIdO,
+          for (int k = 0; k < kBN / 16; ++k)  // 16 keys (2048 bytes of V) per instruction
+            mma_bf16_ts(d, a + k * 8, b + static_cast<uint64_t>(k * (2048 >> 4)), kIdO,
                         (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(bar(Lay::bPV + t));
           if (j == n_kv[t] - 1) mma_commit(bar(Lay::bOD + t));
