@@ -317,6 +317,35 @@ def run_ours(args, w, rank, world, dist):
         except Exception as e:  # reported, never silently replaced
             unfused = {"error": str(e)[:200]}
 
+    # ---- grouped-query variant of the same shape (32 query heads sharing 8 K/V heads)
+    gqa = None
+    if not args.no_extras:
+        g = configs.GQA
+        gq, gk, gv, _ = g.make()
+        gq, gk, gv = to_dev(gq), to_dev(gk), to_dev(gv)
+        go = torch.empty_like(gq)
+        gl = torch.empty(gq.shape[:-1], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            attn.attn_fwd(gq, gk, gv, causal=g.causal, scale=g.scale, out=go, lse=gl)
+        barrier()
+        n_g = 50
+        g_ms = []
+        for _ in range(n_g):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.attn_fwd(gq, gk, gv, causal=g.causal, scale=g.scale, out=go, lse=gl)
+            e1.record(stream)
+            g_ms.append((e0, e1))
+        barrier()
+        g_ms = statistics.mean(a.elapsed_time(b) for a, b in g_ms)
+        g_flops = acc.attention_flops(g.H, [g.N] * g.B, g.d, g.causal)
+        gqa = {"workload": g.name, "ms": g_ms, "tflops": g_flops / (g_ms * 1e-3) / 1e12,
+               "frac_of_peak": g_flops / (g_ms * 1e-3) / 1e12 / peak,
+               "kv_bytes_saved": 2 * (g.H - g.kv_heads) * g.B * g.N * g.d * 2}
+        del gq, gk, gv, go, gl
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
@@ -335,6 +364,7 @@ def run_ours(args, w, rank, world, dist):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "unfused": unfused,
+            "gqa": gqa,
             "clocks": clock_info, "gpu_launches": args.steps,
             "kernel_ms_median": statistics.median(per),
         }
@@ -352,6 +382,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the grouped-query measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

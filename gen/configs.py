@@ -35,6 +35,7 @@ class Workload:
     sigma_qk: float = 1.0
     sigma_v: float = 1.0
     varlen: bool = False
+    H_kv: int = 0    # key/value heads (0: same as H); H_kv < H is grouped-query attention
     n_seqs: int = 0
     len_lo: int = 0
     len_hi: int = 0
@@ -59,13 +60,18 @@ class Workload:
     def total_tokens(self) -> int:
         return int(self.lengths().sum()) if self.varlen else self.B * self.N
 
-    def shape(self) -> tuple:
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
+
+    def shape(self, heads=None) -> tuple:
+        h = self.H if heads is None else heads
         if self.varlen:
-            return (self.H, self.total_tokens(), self.d)
-        return (self.B, self.H, self.N, self.d)
+            return (h, self.total_tokens(), self.d)
+        return (self.B, h, self.N, self.d)
 
     def describe(self) -> dict:
-        out = {"workload": self.name, "heads": self.H, "head_dim": self.d,
+        out = {"workload": self.name, "heads": self.H, "kv_heads": self.kv_heads, "head_dim": self.d,
                "causal": self.causal, "sigma_qk": self.sigma_qk, "sigma_v": self.sigma_v}
         if self.varlen:
             out.update({"layout": "packed [H,T,d] + cu_seqlens", "n_seqs": self.n_seqs,
@@ -76,11 +82,13 @@ class Workload:
         return out
 
     def make(self, shape=None):
-        """(q, k, v) as uint16 bf16 bit arrays, plus cu_seqlens (int32) or None."""
-        shape = self.shape() if shape is None else shape
-        q = inputs.bf16_normal(3 * self.seed + 0, shape, self.sigma_qk)
-        k = inputs.bf16_normal(3 * self.seed + 1, shape, self.sigma_qk)
-        v = inputs.bf16_normal(3 * self.seed + 2, shape, self.sigma_v)
+        """(q, k, v) as uint16 bf16 bit arrays, plus cu_seqlens (int32) or None.  K and V have
+        ``kv_heads`` heads."""
+        qshape = self.shape() if shape is None else shape
+        kvshape = self.shape(self.kv_heads) if shape is None else shape
+        q = inputs.bf16_normal(3 * self.seed + 0, qshape, self.sigma_qk)
+        k = inputs.bf16_normal(3 * self.seed + 1, kvshape, self.sigma_qk)
+        v = inputs.bf16_normal(3 * self.seed + 2, kvshape, self.sigma_v)
         return q, k, v, self.cu_seqlens()
 
 
@@ -97,21 +105,25 @@ WORKLOADS = {
 # The headline throughput workload (B=2, H=32, N=4096, d=128, non-causal).
 HEADLINE = 3
 
+# Grouped-query variant of the headline shape (32 query heads sharing 8 K/V heads).
+GQA = Workload(6, "B2-H32-KV8-N4096-d128", B=2, H=32, N=4096, d=128, causal=False, H_kv=8)
+
 
 def custom(index_seed: int, B: int, H: int, N: int, d: int, causal: bool,
-           sigma_qk: float = 1.0, sigma_v: float = 1.0) -> Workload:
+           sigma_qk: float = 1.0, sigma_v: float = 1.0, H_kv: int = 0) -> Workload:
     """A dense workload with the same recipe and an arbitrary seed (edge-shape tests)."""
-    return Workload(index_seed, f"B{B}-H{H}-N{N}-d{d}{'-causal' if causal else ''}",
-                    B=B, H=H, N=N, d=d, causal=causal, sigma_qk=sigma_qk, sigma_v=sigma_v)
+    kv = f"-KV{H_kv}" if H_kv else ""
+    return Workload(index_seed, f"B{B}-H{H}{kv}-N{N}-d{d}{'-causal' if causal else ''}",
+                    B=B, H=H, N=N, d=d, causal=causal, sigma_qk=sigma_qk, sigma_v=sigma_v,
+                    H_kv=H_kv)
 
 
-def custom_varlen(index_seed: int, lengths, H: int, d: int, causal: bool) -> tuple:
-    """Packed inputs for explicit lengths: (q, k, v, cu_seqlens) bit arrays."""
+def custom_varlen(index_seed: int, lengths, H: int, d: int, causal: bool, H_kv: int = 0) -> tuple:
+    """Packed inputs for explicit lengths: (q, k, v, cu_seqlens) bit arrays (K/V with H_kv heads)."""
     lengths = np.asarray(lengths, dtype=np.int64)
     T = int(lengths.sum())
     seed = 20260000 + index_seed
-    shape = (H, T, d)
-    q = inputs.bf16_normal(3 * seed + 0, shape)
-    k = inputs.bf16_normal(3 * seed + 1, shape)
-    v = inputs.bf16_normal(3 * seed + 2, shape)
+    q = inputs.bf16_normal(3 * seed + 0, (H, T, d))
+    k = inputs.bf16_normal(3 * seed + 1, (H_kv or H, T, d))
+    v = inputs.bf16_normal(3 * seed + 2, (H_kv or H, T, d))
     return q, k, v, inputs.cu_seqlens_from_lengths(lengths)

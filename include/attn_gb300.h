@@ -82,6 +82,19 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
              void* stream);
 
 /*
+ * Grouped-query / multi-query forward (CS336 Lecture 5 notes, section 6.3: several query heads
+ * share one K/V head).  As attn_fwd, except that k and v have H_kv heads and query head h reads
+ * K/V head h / (H / H_kv):
+ *   dense : q, o [B, H, N, d]; k, v [B, H_kv, N, d]; lse [B, H, N]
+ *   packed: q, o [H, T, d];    k, v [H_kv, T, d];    lse [H, T]
+ * H_kv must divide H (H_kv = H is attn_fwd; H_kv = 1 is multi-query attention), else
+ * ATTN_ERR_SHAPE.  Returns an attn_status.
+ */
+ATTN_API int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* cu_seqlens, int B, int H, int H_kv, int N, int d,
+                          int causal, float scale, void* stream);
+
+/*
  * Unfused comparison path (the "standard attention" of the pages: S written to HBM, read back for
  * the softmax, P written to HBM, read back for P V; CS336 GPU/attention notes, "Attention 为什么
  * 容易 memory-bound"; CS336 Lecture 5 notes, section 6.1).  Three kernel launches on `stream`:

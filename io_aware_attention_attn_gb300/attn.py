@@ -26,6 +26,7 @@ STATUS = {
 _P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_unfused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_fwd_unfused_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_fwd_unfused_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -73,13 +74,21 @@ def _stream_handle(stream, device):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _check_inputs(q, k, v, cu_seqlens):
+def _check_inputs(q, k, v, cu_seqlens, allow_kv_heads=False):
+    """Returns (B, H, H_kv, N, d).  K and V may have fewer heads than Q when allow_kv_heads."""
     import torch
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
-        if t.shape != q.shape or t.device != q.device:
-            raise ValueError("q, k and v must have the same shape and device")
+        if t.dim() != q.dim() or t.device != q.device:
+            raise ValueError("q, k and v must have the same rank and device")
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    hd = 1 if cu_seqlens is None else 0  # index of the head axis
+    if q.shape[:hd] + q.shape[hd + 1:] != k.shape[:hd] + k.shape[hd + 1:]:
+        raise ValueError("q and k/v differ in a dimension other than heads")
+    if not allow_kv_heads and k.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape")
     if cu_seqlens is None:
         if q.dim() != 4:
             raise ValueError("dense inputs are [B, H, N, d]")
@@ -93,26 +102,37 @@ def _check_inputs(q, k, v, cu_seqlens):
             raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor on q's device")
         H, N, d = q.shape
         B = cu_seqlens.numel() - 1
-    return B, H, N, d
+    H_kv = k.shape[hd]
+    if H_kv == 0 or H % H_kv != 0:
+        raise ValueError("the number of K/V heads must divide the number of query heads")
+    return B, H, H_kv, N, d
 
 
 def attn_fwd(q, k, v, cu_seqlens=None, causal: bool = False, scale: float | None = None,
              out=None, lse=None, stream=None):
-    """Fused attention forward.  Returns (O bf16 like q, LSE fp32)."""
+    """Fused attention forward.  Returns (O bf16 like q, LSE fp32).
+
+    k and v may have fewer heads than q (grouped-query / multi-query attention: query head h
+    reads K/V head h // (H // H_kv)); then the attn_fwd_gqa entry point is called."""
     import torch
-    B, H, N, d = _check_inputs(q, k, v, cu_seqlens)
+    B, H, H_kv, N, d = _check_inputs(q, k, v, cu_seqlens, allow_kv_heads=True)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    cu = cu_seqlens.data_ptr() if cu_seqlens is not None else None
     with torch.cuda.device(q.device):
-        rc = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                            lse.data_ptr(), cu_seqlens.data_ptr() if cu_seqlens is not None else None,
-                            B, H, N, d, int(bool(causal)), float(scale),
-                            _stream_handle(stream, q.device))
-    _check("attn_fwd", rc)
+        st = _stream_handle(stream, q.device)
+        if H_kv == H:
+            rc = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), cu, B, H, N, d, int(bool(causal)), float(scale), st)
+        else:
+            rc = lib().attn_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), cu, B, H, H_kv, N, d, int(bool(causal)),
+                                    float(scale), st)
+    _check("attn_fwd_gqa" if H_kv != H else "attn_fwd", rc)
     return out, lse
 
 
@@ -124,7 +144,7 @@ def attn_fwd_unfused(q, k, v, causal: bool = False, scale: float | None = None, 
                      out=None, lse=None, stream=None):
     """Unfused three-kernel comparison path (S and P through HBM).  Dense layout only."""
     import torch
-    B, H, N, d = _check_inputs(q, k, v, None)
+    B, H, _, N, d = _check_inputs(q, k, v, None)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     need = unfused_workspace_bytes(B, H, N, d)
@@ -149,7 +169,7 @@ def attn_fwd_unfused_noalloc(q, k, v, causal: bool = False, scale: float | None 
     """The unfused path using the library's built-in scratch instead of a workspace (for callers
     that cannot allocate device memory; outputs may still be allocated here when not given)."""
     import torch
-    B, H, N, d = _check_inputs(q, k, v, None)
+    B, H, _, N, d = _check_inputs(q, k, v, None)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:

@@ -120,23 +120,22 @@ static int validate(const void* q, const void* k, const void* v, const void* o, 
   return ATTN_OK;
 }
 
-}  // namespace attn
-
-using namespace attn;
-
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                        const int32_t* cu_seqlens, int B, int H, int N, int d, int causal,
-                        float scale, void* stream) {
+static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* cu_seqlens, int B, int H, int Hkv, int N, int d, int causal,
+                    float scale, void* stream) {
   bool empty = false;
   int rc = validate(q, k, v, o, lse, cu_seqlens, B, H, N, d, scale, &empty);
-  if (rc != ATTN_OK || empty) return rc;
+  if (rc != ATTN_OK) return rc;
+  if (Hkv < 0 || (H > 0 && (Hkv == 0 || H % Hkv != 0))) return ATTN_ERR_SHAPE;
+  if (empty) return ATTN_OK;
   if ((rc = check_device()) != 0) return rc;
   FwdParams p{};
   const bool varlen = cu_seqlens != nullptr;
-  const uint64_t heads = varlen ? static_cast<uint64_t>(H) : static_cast<uint64_t>(B) * H;
-  if (encode_rows_map(&p.tm_q, q, d, N, heads) != CUDA_SUCCESS ||
-      encode_rows_map(&p.tm_k, k, d, N, heads) != CUDA_SUCCESS ||
-      encode_rows_map(&p.tm_v, v, d, N, heads) != CUDA_SUCCESS)
+  const uint64_t q_heads = varlen ? static_cast<uint64_t>(H) : static_cast<uint64_t>(B) * H;
+  const uint64_t kv_heads = varlen ? static_cast<uint64_t>(Hkv) : static_cast<uint64_t>(B) * Hkv;
+  if (encode_rows_map(&p.tm_q, q, d, N, q_heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_k, k, d, N, kv_heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_v, v, d, N, kv_heads) != CUDA_SUCCESS)
     return ATTN_ERR_LAUNCH;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -146,6 +145,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.B = B;
   p.H = H;
   p.N = N;
+  p.group = H / Hkv;
   p.n_qt = (N + 2 * kBM - 1) / (2 * kBM);  // pairs of 128-row query tiles per head
   p.scale_log2 = scale * 1.4426950408889634f;
   const int grid = varlen ? (p.n_qt + B) * H : p.n_qt * B * H;
@@ -153,6 +153,22 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   const cudaError_t e = (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, grid, st)
                                   : launch_fwd_d128(p, causal != 0, varlen, grid, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens, int B, int H, int N, int d, int causal,
+                        float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, cu_seqlens, B, H, H, N, d, causal, scale, stream);
+}
+
+extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens, int B, int H, int H_kv, int N, int d,
+                            int causal, float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, cu_seqlens, B, H, H_kv, N, d, causal, scale, stream);
 }
 
 extern "C" int attn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,

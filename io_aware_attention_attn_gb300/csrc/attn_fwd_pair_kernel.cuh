@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     n_kv[t] = (qt * kBM >= seq_len) ? 0 : (CAUSAL ? qt + 1 : n_keytiles);
   }
   const int n_max = n_kv[0] > n_kv[1] ? n_kv[0] : n_kv[1];
+  // K/V head slice: query head h reads K/V head h / group (grouped-query attention); dense maps
+  // are indexed by batch * heads + head, packed maps by head
+  const int z_kv = VARLEN ? z / p.group : (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
 
   if (warp == 0) {
     // ===================================================================== TMA producer
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kK + sk * Lay::kTile + c * 16384, &p.tm_k,
-                           bar(Lay::bKF + sk), c * 64, y0 + j * kBN, z, keep);
+                           bar(Lay::bKF + sk), c * 64, y0 + j * kBN, z_kv, keep);
         ++nk;
         if (j >= kPairStagesV &&
             !(ok = mbar_wait(bar(Lay::bVE + sv),
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kV + sv * Lay::kTile + c * 16384, &p.tm_v,
-                           bar(Lay::bVF + sv), c * 64, y0 + j * kBN, z, keep);
+                           bar(Lay::bVF + sv), c * 64, y0 + j * kBN, z_kv, keep);
         ++nv;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits

@@ -22,7 +22,8 @@ struct FwdParams {
   float* lse;
   const int* cu_seqlens;     // packed layout only
   int* status;               // device status word (bounded-wait failures)
-  int B, H, N;               // N: sequence length (dense) or total tokens T (packed)
+  int B, H, N;               // H: query heads; N: sequence length (dense) or total tokens T
+  int group;                 // query heads per K/V head (1: multi-head; H: multi-query)
   int n_qt;                  // dense: query-tile pairs (256 rows) per head
   float scale_log2;          // scale * log2(e)
 };

@@ -117,6 +117,44 @@ def attention_varlen(q, k, v, cu_seqlens, causal: bool, scale: float):
     return o, lse
 
 
+def attention_gqa_dense(q, k, v, causal: bool, scale: float, heads=None):
+    """Grouped-query attention, dense: q [B, H, N, d], k and v [B, H_kv, N, d] with H_kv | H.
+
+    Query head h attends with key/value head h // (H // H_kv): several query heads share one K/V
+    head (CS336 Lecture 5 notes, section 6.3, "MQA / GQA"); H_kv = 1 is multi-query attention.
+    Returns (O [B,H,N,d], LSE [B,H,N]); ``heads``: optional (b, h) pairs to compute (others NaN).
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, N, d = q.shape
+    group = H // k.shape[1]
+    o = np.full((B, H, N, d), np.nan)
+    lse = np.full((B, H, N), np.nan)
+    todo = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in todo:
+        o[b, h], lse[b, h] = attention_head_rows(q[b, h], k[b, h // group], v[b, h // group],
+                                                 np.arange(N), causal, scale)
+    return o, lse
+
+
+def attention_gqa_varlen(q, k, v, cu_seqlens, causal: bool, scale: float):
+    """Grouped-query attention on a packed batch: q [H, T, d], k and v [H_kv, T, d]."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    H, T, d = q.shape
+    group = H // k.shape[0]
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    o = np.full((H, T, d), np.nan)
+    lse = np.full((H, T), np.nan)
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b == a:
+            continue
+        for h in range(H):
+            o[h, a:b], lse[h, a:b] = attention_head_rows(q[h, a:b], k[h // group, a:b],
+                                                         v[h // group, a:b], np.arange(b - a),
+                                                         causal, scale)
+    return o, lse
+
+
 def probabilities(q, k, causal: bool, scale: float) -> np.ndarray:
     """The full probability matrix P = softmax(scale * q k^T) of one head ([L, L]; small L)."""
     q, k = _as_f64(q), _as_f64(k)

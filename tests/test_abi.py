@@ -97,3 +97,13 @@ def test_selftest_validation(lib):
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 0, 32, None) == -2
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 7, 64, None) == -9
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, -1, 64, None) == -9
+
+
+def test_gqa_validation(lib):
+    f = lib.attn_fwd_gqa
+    A = ALIGNED
+    assert f(A, A, A, A, A, None, 1, 8, 3, 128, 128, 0, 0.1, None) == -3   # 3 does not divide 8
+    assert f(A, A, A, A, A, None, 1, 8, 0, 128, 128, 0, 0.1, None) == -3
+    assert f(A, A, A, A, A, None, 1, 8, -1, 128, 128, 0, 0.1, None) == -3
+    assert f(A, A, A, A, A, None, 1, 8, 2, 128, 96, 0, 0.1, None) == -2
+    assert f(A, A, A, A, A, None, 1, 0, 0, 128, 128, 0, 0.1, None) == 0    # nothing to do

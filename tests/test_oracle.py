@@ -271,3 +271,53 @@ def test_bf16_decode_exact():
     bits = np.array([0x3F80, 0xBF80, 0x0000, 0x8000, 0x4049, 0x7F7F, 0x0001], dtype=np.uint16)
     want = [1.0, -1.0, 0.0, -0.0, 3.140625, 3.3895313892515355e38, 9.183549615799121e-41]
     assert orc.bf16_bits_to_f64(bits).tolist() == want
+
+
+# ------------------------------------------------------------- grouped-query attention
+def _gqa_inputs(seed, B, H, H_kv, N, d):
+    w = configs.custom(seed, B, H, N, d, False, H_kv=H_kv)
+    q, k, v, _ = w.make()
+    return q, k, v
+
+
+def test_gqa_with_all_heads_is_multi_head():
+    q, k, v = _gqa_inputs(60, 2, 4, 4, 50, 16)
+    for causal in (False, True):
+        a = orc.attention_gqa_dense(q, k, v, causal, 0.3)
+        b = orc.attention_dense(q, k, v, causal, 0.3)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("H_kv", [1, 2, 3])
+def test_gqa_equals_multi_head_on_repeated_kv(H_kv):
+    H = 6
+    q, k, v = _gqa_inputs(61, 2, H, H_kv, 40, 8)
+    rk, rv = np.repeat(k, H // H_kv, axis=1), np.repeat(v, H // H_kv, axis=1)
+    for causal in (False, True):
+        a = orc.attention_gqa_dense(q, k, v, causal, 0.35)
+        b = orc.attention_dense(q, rk, rv, causal, 0.35)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_gqa_interleaved_grouping_is_caught():
+    # planted mistake: query head h reading K/V head h % H_kv instead of h // (H / H_kv)
+    q, k, v = _gqa_inputs(62, 1, 4, 2, 30, 8)
+    good = orc.attention_gqa_dense(q, k, v, False, 0.4)[0]
+    wrong = np.stack([orc.attention_head_rows(q[0, h], k[0, h % 2], v[0, h % 2], np.arange(30),
+                                              False, 0.4)[0] for h in range(4)])[None]
+    rk, rv = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    ref = orc.attention_dense(q, rk, rv, False, 0.4)[0]
+    assert np.array_equal(good, ref) and not np.allclose(wrong, ref)
+
+
+def test_gqa_varlen_matches_dense_per_sequence():
+    lengths = [7, 0, 65]
+    q, k, v, cu = configs.custom_varlen(63, lengths, 4, 8, True, H_kv=2)
+    o, lse = orc.attention_gqa_varlen(q, k, v, cu, True, 0.5)
+    for s, L in enumerate(lengths):
+        a = int(cu[s])
+        if L == 0:
+            continue
+        od, ld = orc.attention_gqa_dense(q[None, :, a:a + L], k[None, :, a:a + L],
+                                         v[None, :, a:a + L], True, 0.5)
+        assert np.allclose(o[:, a:a + L], od[0], atol=1e-14) and np.allclose(lse[:, a:a + L], ld[0], atol=1e-14)
