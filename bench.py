@@ -346,6 +346,46 @@ def run_ours(args, w, rank, world, dist):
                "kv_bytes_saved": 2 * (g.H - g.kv_heads) * g.B * g.N * g.d * 2}
         del gq, gk, gv, go, gl
 
+    # ---- split-KV on a few-heads, long-sequence shape (64 query pairs for 152 SMs): the
+    # library's slice count against one slice (the plain fused kernel)
+    splitkv = None
+    if not args.no_extras:
+        sw = configs.SPLITKV
+        sq, sk, sv, _ = sw.make()
+        sq, sk, sv = to_dev(sq), to_dev(sk), to_dev(sv)
+        so = torch.empty_like(sq)
+        sl = torch.empty(sq.shape[:-1], dtype=torch.float32, device=dev)
+        need = attn.splitkv_workspace_bytes(sw.B, sw.H, sw.N, sw.d, 0)
+        sws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        s_flops = acc.attention_flops(sw.H, [sw.N] * sw.B, sw.d, sw.causal)
+
+        def time_split(n_splits, n=50):
+            for _ in range(3):
+                attn.attn_fwd_splitkv(sq, sk, sv, causal=sw.causal, scale=sw.scale,
+                                      num_splits=n_splits, workspace=sws, out=so, lse=sl)
+            barrier()
+            evs = []
+            for _ in range(n):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                attn.attn_fwd_splitkv(sq, sk, sv, causal=sw.causal, scale=sw.scale,
+                                      num_splits=n_splits, workspace=sws, out=so, lse=sl)
+                e1.record(stream)
+                evs.append((e0, e1))
+            barrier()
+            return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+        ms_auto = time_split(0)
+        ms_one = time_split(1)
+        chosen = attn.splitkv_slices(sw.B, sw.H, sw.N, 0)
+        splitkv = {"workload": sw.name, "splits": chosen, "ms": ms_auto,
+                   "tflops": s_flops / (ms_auto * 1e-3) / 1e12, "ms_one_slice": ms_one,
+                   "tflops_one_slice": s_flops / (ms_one * 1e-3) / 1e12,
+                   "speedup": ms_one / ms_auto, "launches_per_step": 2 if chosen > 1 else 1}
+        del sq, sk, sv, so, sl, sws
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
@@ -364,7 +404,7 @@ def run_ours(args, w, rank, world, dist):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "unfused": unfused,
-            "gqa": gqa,
+            "gqa": gqa, "splitkv": splitkv,
             "clocks": clock_info, "gpu_launches": args.steps,
             "kernel_ms_median": statistics.median(per),
         }
@@ -383,7 +423,7 @@ def main():
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the grouped-query measurement")
+                    help="skip the grouped-query and split-KV measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

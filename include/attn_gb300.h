@@ -95,6 +95,41 @@ ATTN_API int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
                           int causal, float scale, void* stream);
 
 /*
+ * Split-KV forward for problems with few query tiles (small B * H): the key/value sequence of
+ * every pair of query tiles is cut into num_splits contiguous slices, one CTA per slice, so that
+ * more SMs share the work (sequence-dimension parallelism, CS336 Lecture 5 notes, section 6.3).
+ * Each slice leaves its unnormalised output, its reference row maximum and its row sums in
+ * `workspace`; a second kernel on `stream` merges the slices with the block merge of the CS336
+ * GPU/attention notes, "Online softmax 回顾" (M = max of the slice maxima, each slice weighted by
+ * exp(m_s - M), O = sum of weighted outputs / sum of weighted sums, lse = M + ln(weighted sum)).
+ * Dense layout only: q, k, v, o [B, H, N, d] bf16, lse [B, H, N] fp32, as attn_fwd.
+ *   num_splits : slices per query pair, at most 32 and at most the number of 128-key tiles
+ *                (larger values are lowered).  <= 0 lets the library choose: the count that
+ *                minimises (waves of 152 CTAs) x (key tiles per slice + 2), the smallest on ties.
+ *                When the count is 1 this is attn_fwd and the workspace is not touched.
+ *   workspace  : caller-owned device buffer of at least
+ *                attn_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) bytes, 256-byte
+ *                aligned, else ATTN_ERR_WORKSPACE; its contents on return are unspecified.
+ * Returns an attn_status (argument checks as attn_fwd).
+ */
+ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int N, int d, int causal, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The slice count attn_fwd_splitkv uses for these sizes and num_splits (0 for invalid sizes).
+ */
+ATTN_API int attn_fwd_splitkv_slices(int B, int H, int N, int num_splits);
+
+/*
+ * Workspace bytes attn_fwd_splitkv needs: with S the slice count it will use, an fp32 partial
+ * output [S][B*H*N][d] followed by three fp32 planes [3][S][B*H*N] (slice max in log2 units, the
+ * exact row sum, the row sum of the bf16-rounded weights), each region rounded up to 256 bytes.
+ * Returns 0 when S is 1 (no workspace needed) or the sizes are invalid.
+ */
+ATTN_API size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
+
+/*
  * Unfused comparison path (the "standard attention" of the pages: S written to HBM, read back for
  * the softmax, P written to HBM, read back for P V; CS336 GPU/attention notes, "Attention 为什么
  * 容易 memory-bound"; CS336 Lecture 5 notes, section 6.1).  Three kernel launches on `stream`:

@@ -27,6 +27,9 @@ _P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "attn_fwd_splitkv_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
+    "attn_fwd_splitkv_slices": (_I, [_I, _I, _I, _I]),
     "attn_fwd_unfused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_fwd_unfused_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_fwd_unfused_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -133,6 +136,40 @@ def attn_fwd(q, k, v, cu_seqlens=None, causal: bool = False, scale: float | None
                                     lse.data_ptr(), cu, B, H, H_kv, N, d, int(bool(causal)),
                                     float(scale), st)
     _check("attn_fwd_gqa" if H_kv != H else "attn_fwd", rc)
+    return out, lse
+
+
+def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int = 0) -> int:
+    return int(lib().attn_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits))
+
+
+def splitkv_slices(B: int, H: int, N: int, num_splits: int = 0) -> int:
+    return int(lib().attn_fwd_splitkv_slices(B, H, N, num_splits))
+
+
+def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
+                     num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
+    """Split-KV fused forward (dense [B, H, N, d] only): the key range of every query pair is
+    cut into ``num_splits`` slices (0: the library chooses) whose partial results a second kernel
+    merges.  Returns (O bf16 like q, LSE fp32)."""
+    import torch
+    B, H, _, N, d = _check_inputs(q, k, v, None)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = splitkv_workspace_bytes(B, H, N, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                    int(num_splits), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream, q.device))
+    _check("attn_fwd_splitkv", rc)
     return out, lse
 
 

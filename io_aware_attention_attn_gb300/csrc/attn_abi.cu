@@ -122,7 +122,8 @@ static int validate(const void* q, const void* k, const void* v, const void* o, 
 
 static int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
                     const int32_t* cu_seqlens, int B, int H, int Hkv, int N, int d, int causal,
-                    float scale, void* stream) {
+                    float scale, void* stream, int n_splits = 1, float* part_o = nullptr,
+                    float* part_stat = nullptr) {
   bool empty = false;
   int rc = validate(q, k, v, o, lse, cu_seqlens, B, H, N, d, scale, &empty);
   if (rc != ATTN_OK) return rc;
@@ -146,13 +147,28 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.H = H;
   p.N = N;
   p.group = H / Hkv;
+  p.n_splits = n_splits;
+  p.part_o = part_o;
+  p.part_stat = part_stat;
   p.n_qt = (N + 2 * kBM - 1) / (2 * kBM);  // pairs of 128-row query tiles per head
   p.scale_log2 = scale * 1.4426950408889634f;
-  const int grid = varlen ? (p.n_qt + B) * H : p.n_qt * B * H;
+  const long long grid = varlen ? static_cast<long long>(p.n_qt + B) * H
+                                 : static_cast<long long>(p.n_qt) * B * H * n_splits;
+  if (grid > INT_MAX) return ATTN_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, grid, st)
-                                  : launch_fwd_d128(p, causal != 0, varlen, grid, st);
+  cudaError_t e = (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, static_cast<int>(grid), st)
+                            : launch_fwd_d128(p, causal != 0, varlen, static_cast<int>(grid), st);
+  if (e == cudaSuccess && n_splits > 1)
+    e = launch_splitkv_combine(d, part_o, part_stat, o, lse, static_cast<long long>(B) * H * N,
+                               n_splits, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// Split-KV workspace: partial O [S][B H N][d] fp32, then [3][S][B H N] fp32 statistics.
+static size_t splitkv_bytes(int B, int H, int N, int d, int S) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t o_bytes = (static_cast<size_t>(S) * rows * d * 4 + 255) / 256 * 256;
+  return o_bytes + (3 * static_cast<size_t>(S) * rows * 4 + 255) / 256 * 256;
 }
 
 }  // namespace attn
@@ -169,6 +185,38 @@ extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o
                             const int32_t* cu_seqlens, int B, int H, int H_kv, int N, int d,
                             int causal, float scale, void* stream) {
   return fwd_impl(q, k, v, o, lse, cu_seqlens, B, H, H_kv, N, d, causal, scale, stream);
+}
+
+extern "C" int attn_fwd_splitkv_slices(int B, int H, int N, int num_splits) {
+  if (B <= 0 || H <= 0 || N <= 0) return 0;
+  return splitkv_pick(B, H, N, num_splits);
+}
+
+extern "C" size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  const int S = splitkv_pick(B, H, N, num_splits);
+  return S > 1 ? splitkv_bytes(B, H, N, d, S) : 0;
+}
+
+extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int N, int d, int causal, float scale,
+                                int num_splits, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  bool empty = false;
+  const int rc = validate(q, k, v, o, lse, nullptr, B, H, N, d, scale, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  const int S = splitkv_pick(B, H, N, num_splits);
+  if (S == 1) return fwd_impl(q, k, v, o, lse, nullptr, B, H, H, N, d, causal, scale, stream);
+  const size_t need = splitkv_bytes(B, H, N, d, S);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  float* part_o = static_cast<float*>(workspace);
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  float* part_stat = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                              (static_cast<size_t>(S) * rows * d * 4 + 255) /
+                                                  256 * 256);
+  return fwd_impl(q, k, v, o, lse, nullptr, B, H, H, N, d, causal, scale, stream, S, part_o,
+                  part_stat);
 }
 
 extern "C" int attn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -83,9 +83,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   // ---- which pair of query tiles this CTA owns: z = head slice of the tensor maps, y0 = first row
   // of the sequence along the maps' row axis, pt = pair index within the sequence
   int z, y0, seq_len, pt;
+  // split-KV (dense only): consecutive CTAs are the slices of one query pair
+  const int split = VARLEN ? 0 : static_cast<int>(blockIdx.x) % p.n_splits;
   if constexpr (!VARLEN) {
     const int BH = p.B * p.H;
-    const int L = blockIdx.x;
+    const int L = static_cast<int>(blockIdx.x) / p.n_splits;
     if constexpr (CAUSAL) {  // heaviest pairs (most key tiles) first
       pt = p.n_qt - 1 - L / BH;
       z = L % BH;
@@ -147,6 +149,40 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (pt < 0) return;  // slot beyond the last pair of the batch (uniform for the CTA)
   }
 
+  // key tiles each query tile visits (0 if the tile starts past the end of the sequence); with
+  // split-KV this CTA takes key tiles [kb, kb + chunk) of the pair's range, and n_kv[t] counts
+  // the tiles of that slice query tile t visits.  Pipeline bookkeeping runs over j = 0..n_kv-1;
+  // key tile kb + j is the data.
+  const int n_keytiles = (seq_len + kBN - 1) / kBN;
+  int n_full[2];
+  #pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = 2 * pt + t;
+    n_full[t] = (qt * kBM >= seq_len) ? 0 : (CAUSAL ? qt + 1 : n_keytiles);
+  }
+  const int n_full_max = n_full[0] > n_full[1] ? n_full[0] : n_full[1];
+  const int chunk = (n_full_max + p.n_splits - 1) / p.n_splits;
+  const int kb = split * chunk;
+  int n_kv[2];
+  #pragma unroll
+  for (int t = 0; t < 2; ++t) n_kv[t] = max(0, min(kb + chunk, n_full[t]) - kb);
+  const int n_max = n_kv[0] > n_kv[1] ? n_kv[0] : n_kv[1];
+  if (!VARLEN && p.n_splits > 1 && n_max == 0) {
+    // a key slice past the end of this pair's range: nothing to load or multiply; the merge
+    // reads max -inf and sums 0 for its rows (uniform for the CTA, before any copy is issued)
+    const size_t rows_total = static_cast<size_t>(p.B) * p.H * p.N;
+    const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
+    const int row = 2 * pt * kBM + static_cast<int>(threadIdx.x);
+    if (threadIdx.x < 2 * kBM && row < seq_len) {
+      const size_t slot = static_cast<size_t>(split) * rows_total +
+                          static_cast<size_t>(z) * static_cast<size_t>(p.N) + row;
+      p.part_stat[slot] = -INFINITY;
+      p.part_stat[plane + slot] = 0.f;
+      p.part_stat[2 * plane + slot] = 0.f;
+    }
+    return;
+  }
+
   if (warp == 1) {
     tmem_alloc(sbase + Lay::kMisc, 512);
     tmem_relinquish();
@@ -158,15 +194,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   constexpr uint32_t kColS[2] = {0, 128};
   constexpr uint32_t kColO[2] = {256, 256 + D};
 
-  // key tiles each query tile visits (0 if the tile starts past the end of the sequence)
-  const int n_keytiles = (seq_len + kBN - 1) / kBN;
-  int n_kv[2];
-  #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qt = 2 * pt + t;
-    n_kv[t] = (qt * kBM >= seq_len) ? 0 : (CAUSAL ? qt + 1 : n_keytiles);
-  }
-  const int n_max = n_kv[0] > n_kv[1] ? n_kv[0] : n_kv[1];
   // K/V head slice: query head h reads K/V head h / group (grouped-query attention); dense maps
   // are indexed by batch * heads + head, packed maps by head
   const int z_kv = VARLEN ? z / p.group : (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
@@ -198,7 +225,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kK + sk * Lay::kTile + c * 16384, &p.tm_k,
-                           bar(Lay::bKF + sk), c * 64, y0 + j * kBN, z_kv, keep);
+                           bar(Lay::bKF + sk), c * 64, y0 + (kb + j) * kBN, z_kv, keep);
         ++nk;
         if (j >= kPairStagesV &&
             !(ok = mbar_wait(bar(Lay::bVE + sv),
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kV + sv * Lay::kTile + c * 16384, &p.tm_v,
-                           bar(Lay::bVF + sv), c * 64, y0 + j * kBN, z_kv, keep);
+                           bar(Lay::bVF + sv), c * 64, y0 + (kb + j) * kBN, z_kv, keep);
         ++nv;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
@@ -252,7 +279,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (ok) {
       tc_fence_after();
       if (lane == 0) {
-        issue_s(0, 0);
+        if (n_kv[0] > 0) issue_s(0, 0);  // a key slice may hold no tile of query tile 0
         if (n_kv[1] > 0) issue_s(1, 0);
         mma_commit(bar(Lay::bKE + 0));
       }
@@ -274,7 +301,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           if constexpr (VARLEN) {
             // rows of the last V tile past the end of the sequence belong to the next sequence:
             // zero them so that P = 0 there cannot meet a non-finite value
-            const int valid = seq_len - j * kBN;
+            const int valid = seq_len - (kb + j) * kBN;
             if (valid < kBN) {
               const uint32_t vbase = sbase + Lay::kV + sv * Lay::kTile;
               #pragma unroll
@@ -357,8 +384,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         s[64 + i] = u2f(u2[i]);
         s[96 + i] = u2f(u3[i]);
       }
-      const int key0 = j * kBN;
-      if ((CAUSAL && j == qt) || key0 + kBN > seq_len) {
+      const int key0 = (kb + j) * kBN;
+      if ((CAUSAL && kb + j == qt) || key0 + kBN > seq_len) {
         const int lim = CAUSAL ? min(seq_len - key0, row - key0 + 1) : (seq_len - key0);
         #pragma unroll
         for (int c = 0; c < kBN; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
@@ -422,14 +449,42 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_arrive(bar(Lay::bPF + t));
     }
     if (n > 0 && ok) ok = mbar_wait_warp(bar(Lay::bOD + t), 0, wc, 2, 9);
-    if (n > 0 && ok) {
+    const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
+    const float l_round = (lr[0] + lr[1]) + (lr[2] + lr[3]);
+    const bool valid = row < seq_len;
+    const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
+                        static_cast<size_t>(y0) + static_cast<size_t>(row);
+    if (p.n_splits > 1) {
+      // this key slice's partial result for the merge: unnormalised O, reference max and both
+      // row sums (a slice without keys for this tile contributes max -inf and sums 0)
+      const size_t rows_total = static_cast<size_t>(p.B) * p.H * p.N;
+      const size_t slot = static_cast<size_t>(split) * rows_total + grow;
+      const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
+      const bool has = n > 0 && ok;
+      if (valid) {
+        p.part_stat[slot] = has ? m2 : -INFINITY;
+        p.part_stat[plane + slot] = has ? l_exact : 0.f;
+        p.part_stat[2 * plane + slot] = has ? l_round : 0.f;
+      }
+      if (has) {
+        tc_fence_after();
+        float4* prow = reinterpret_cast<float4*>(p.part_o + slot * D);
+        #pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_col + c * 32, o);
+          tmem_wait_ld_regs(o);
+          if (valid) {
+            #pragma unroll
+            for (int q = 0; q < 8; ++q)
+              prow[c * 8 + q] = make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]),
+                                            u2f(o[4 * q + 3]));
+          }
+        }
+      }
+    } else if (n > 0 && ok) {
       tc_fence_after();
-      const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
-      const float l_round = (lr[0] + lr[1]) + (lr[2] + lr[3]);
-      const bool valid = row < seq_len;
       const float inv_l = 1.f / l_round;
-      const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
-                          static_cast<size_t>(y0) + static_cast<size_t>(row);
       uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);
       #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -449,7 +504,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -24,6 +24,10 @@ struct FwdParams {
   int* status;               // device status word (bounded-wait failures)
   int B, H, N;               // H: query heads; N: sequence length (dense) or total tokens T
   int group;                 // query heads per K/V head (1: multi-head; H: multi-query)
+  int n_splits;              // key-range slices per query pair (1: the whole row in one CTA)
+  float* part_o;             // split-KV partials [n_splits][B H N][D] fp32 (unnormalised O)
+  float* part_stat;          // split-KV partials [3][n_splits][B H N]: reference max (log2),
+                             // exact row sum, rounded row sum
   int n_qt;                  // dense: query-tile pairs (256 rows) per head
   float scale_log2;          // scale * log2(e)
 };
@@ -65,6 +69,33 @@ cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, bool varlen, int gri
                            cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, bool varlen, int grid,
                             cudaStream_t stream);
+
+// Split-KV: slices per query pair the library picks when the caller passes num_splits <= 0, and
+// the merge of the slices' partial results (attn_splitkv.cu).  The pick minimises a simple cost
+// model of the launch: waves of one-CTA-per-SM work (152 SMs) times the key tiles one slice
+// visits plus about two tiles of fixed per-CTA cost (prologue, epilogue, partial write-out).
+constexpr int kSmCount = 152;
+constexpr int kMaxSplits = 32;
+inline int splitkv_pick(int B, int H, int N, int num_splits) {
+  const long long pairs = static_cast<long long>((N + 2 * kBM - 1) / (2 * kBM)) * B * H;
+  const int key_tiles = (N + kBN - 1) / kBN;
+  const int cap = key_tiles < kMaxSplits ? key_tiles : kMaxSplits;
+  if (cap < 1 || pairs < 1) return 1;
+  if (num_splits > 0) return num_splits < cap ? num_splits : cap;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= cap; ++s) {
+    const long long waves = (pairs * s + kSmCount - 1) / kSmCount;
+    const long long cost = waves * ((key_tiles + s - 1) / s + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+cudaError_t launch_splitkv_combine(int d, const float* part_o, const float* part_stat, void* o,
+                                   float* lse, long long rows, int splits, cudaStream_t stream);
 
 // ---------------------------------------------------------------- unfused comparison path
 struct UnfusedArgs {

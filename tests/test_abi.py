@@ -107,3 +107,48 @@ def test_gqa_validation(lib):
     assert f(A, A, A, A, A, None, 1, 8, -1, 128, 128, 0, 0.1, None) == -3
     assert f(A, A, A, A, A, None, 1, 8, 2, 128, 96, 0, 0.1, None) == -2
     assert f(A, A, A, A, A, None, 1, 0, 0, 128, 128, 0, 0.1, None) == 0    # nothing to do
+
+
+def test_splitkv_workspace_bytes(lib):
+    f = lib.attn_fwd_splitkv_workspace_bytes
+    # B=1, H=2, N=8192: 64 query pairs over 64 key tiles; cost(1) = 66, cost(2) = 1 wave x 34,
+    # cost(3) = 2 waves x 24 -> 2 slices
+    rows = 1 * 2 * 8192
+    assert f(1, 2, 8192, 128, 0) == 2 * rows * 128 * 4 + 3 * 2 * rows * 4
+    # B=1, H=1, N=16384: 64 pairs, 128 key tiles; 7 slices (3 waves x 21) beat 2 (1 x 66)
+    rows = 16384
+    assert f(1, 1, 16384, 64, 0) == 7 * rows * 64 * 4 + 3 * 7 * rows * 4
+    assert f(1, 2, 8192, 128, 5) == 5 * 2 * 8192 * 128 * 4 + 3 * 5 * 2 * 8192 * 4
+    # an explicit count above the 8 key tiles of N=1000 is lowered to 8 (regions 256-aligned)
+    rows = 1000
+    o_bytes = -(-8 * rows * 64 * 4 // 256) * 256
+    assert f(1, 1, 1000, 64, 100) == o_bytes + -(-3 * 8 * rows * 4 // 256) * 256
+    assert f(1, 1, 1 << 20, 64, 1000) == 32 * (1 << 20) * 64 * 4 + 3 * 32 * (1 << 20) * 4
+    assert f(1, 2, 8192, 128, 1) == 0        # one slice: plain fused forward, no workspace
+    assert f(2, 32, 4096, 128, 0) == 0       # 1024 pairs already fill the GPU
+    assert f(1, 1, 100, 64, 4) == 0          # a single key tile cannot be split
+    assert f(1, 1, 1000, 96, 2) == 0
+    assert f(0, 1, 1000, 64, 2) == 0
+
+
+def test_splitkv_slices(lib):
+    f = lib.attn_fwd_splitkv_slices
+    assert f(1, 2, 8192, 0) == 2 and f(1, 1, 16384, 0) == 7 and f(2, 32, 4096, 0) == 1
+    assert f(1, 1, 1000, 0) == 8 and f(1, 1, 1000, 3) == 3 and f(1, 1, 1000, 50) == 8
+    assert f(1, 1, 1 << 20, 1000) == 32 and f(1, 1, 100, 0) == 1
+    assert f(0, 1, 100, 0) == 0 and f(1, 1, -5, 0) == 0
+
+
+def test_splitkv_validation(lib):
+    f = lib.attn_fwd_splitkv
+    A = ALIGNED
+    big = 1 << 30
+    assert f(A, A, A, A, A, 1, 2, 8192, 128, 0, 0.1, 4, None, big, None) == -8
+    assert f(A, A, A, A, A, 1, 2, 8192, 128, 0, 0.1, 4, A + 16, big, None) == -8
+    assert f(A, A, A, A, A, 1, 2, 8192, 128, 0, 0.1, 4, A, 1 << 20, None) == -8
+    assert f(A, A, A, A, A, 1, 2, 8192, 96, 0, 0.1, 4, A, big, None) == -2
+    assert f(A, A, A, A, A, 1, 2, 8192, 128, 0, 0.0, 4, A, big, None) == -7
+    assert f(A + 2, A, A, A, A, 1, 2, 8192, 128, 0, 0.1, 4, A, big, None) == -4
+    assert f(None, A, A, A, A, 1, 2, 8192, 128, 0, 0.1, 4, A, big, None) == -1
+    assert f(A, A, A, A, A, -1, 2, 8192, 128, 0, 0.1, 4, A, big, None) == -3
+    assert f(A, A, A, A, A, 0, 2, 8192, 128, 0, 0.1, 4, None, 0, None) == 0
