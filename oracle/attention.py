@@ -214,3 +214,47 @@ def online_softmax_attention(q, k, v, causal: bool, scale: float, block_q: int =
         o[i0:i1] = acc / ell[:, None]
         lse[i0:i1] = m + np.log(ell)
     return o, lse
+
+
+def slice_partials(q, k, v, causal: bool, scale: float, cuts):
+    """Per-slice partial results of one head ([L, d]) for key slices ``cuts[s] .. cuts[s+1]-1``.
+
+    For every slice s and query row: the slice's row maximum ``m_s`` of the scaled visible scores
+    (-inf when the slice holds no visible key), ``l_s = sum exp(s - m_s)`` and the unnormalised
+    output ``a_s = sum exp(s - m_s) v`` -- the (m, l, a) triple of a block in the CS336
+    GPU/attention notes, section "Online softmax 回顾".  Returns arrays m [S, L], l [S, L],
+    a [S, L, d].
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    L, d = q.shape
+    S = len(cuts) - 1
+    m = np.full((S, L), -np.inf)
+    ell = np.zeros((S, L))
+    a = np.zeros((S, L, d))
+    rows = np.arange(L)
+    for s in range(S):
+        j0, j1 = int(cuts[s]), int(cuts[s + 1])
+        if j1 <= j0:
+            continue
+        sc = scale * (q @ k[j0:j1].T)
+        if causal:
+            sc = np.where(np.arange(j0, j1)[None, :] <= rows[:, None], sc, -np.inf)
+        ms = sc.max(axis=1)
+        seen = np.isfinite(ms)
+        e = np.exp(sc[seen] - ms[seen, None])
+        m[s, seen] = ms[seen]
+        ell[s, seen] = e.sum(axis=1)
+        a[s, seen] = e @ v[j0:j1]
+    return m, ell, a
+
+
+def merge_slices(m, ell, a):
+    """Merge per-slice (m, l, a) triples into (O, LSE) by the block merge of the CS336
+    GPU/attention notes, section "Online softmax 回顾", applied to all slices at once:
+    ``M = max_s m_s``, each slice weighted by ``exp(m_s - M)``, ``O = sum w a / sum w l``,
+    ``LSE = M + ln(sum w l)``.  Slices with ``m_s = -inf`` carry weight 0."""
+    M = m.max(axis=0)
+    w = np.where(np.isfinite(m), np.exp(m - np.where(np.isfinite(M), M, 0.0)[None, :]), 0.0)
+    lw = (w * ell).sum(axis=0)
+    o = (w[:, :, None] * a).sum(axis=0) / lw[:, None]
+    return o, M + np.log(lw)

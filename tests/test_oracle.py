@@ -321,3 +321,33 @@ def test_gqa_varlen_matches_dense_per_sequence():
         od, ld = orc.attention_gqa_dense(q[None, :, a:a + L], k[None, :, a:a + L],
                                          v[None, :, a:a + L], True, 0.5)
         assert np.allclose(o[:, a:a + L], od[0], atol=1e-14) and np.allclose(lse[:, a:a + L], ld[0], atol=1e-14)
+
+
+# --------------------------------------------------------- split-KV merge of slices
+@pytest.mark.parametrize("causal", [False, True])
+def test_merged_slices_equal_definition(causal):
+    L, d = 230, 16
+    q = inputs.bf16_normal(21, (L, d), 3.0)
+    k = inputs.bf16_normal(22, (L, d), 3.0)
+    v = inputs.bf16_normal(23, (L, d))
+    # uneven slices, one empty, and (causal) slices that early rows cannot see at all
+    for cuts in ([0, 100, 100, 170, 230], [0, 1, 2, 229, 230], [0, 230]):
+        m, ell, a = orc.slice_partials(q, k, v, causal, 0.3, cuts)
+        o1, l1 = head_fn(q, k, v, causal, 0.3)
+        o2, l2 = orc.merge_slices(m, ell, a)
+        assert np.max(np.abs(o1 - o2)) < 1e-12 and np.max(np.abs(l1 - l2)) < 1e-12
+    if causal:
+        m, _, _ = orc.slice_partials(q, k, v, True, 0.3, [0, 100, 230])
+        assert np.isneginf(m[1, :100]).all() and np.isfinite(m[1, 100:]).all()
+
+
+def test_merge_without_slice_weights_is_caught():
+    # a merge that forgets the exp(m_s - M) weights gives a different answer
+    L, d = 64, 8
+    q = inputs.bf16_normal(24, (L, d), 3.0)
+    k = inputs.bf16_normal(25, (L, d), 3.0)
+    v = inputs.bf16_normal(26, (L, d))
+    m, ell, a = orc.slice_partials(q, k, v, False, 0.5, [0, 20, 64])
+    bad = (a.sum(axis=0)) / ell.sum(axis=0)[:, None]
+    o_ref, _ = head_fn(q, k, v, False, 0.5)
+    assert np.max(np.abs(bad - o_ref)) > 1e-3
