@@ -7,6 +7,7 @@ are bf16 bit patterns from :mod:`gen.inputs`.  Recipe:
   independent splitmix64 streams ``3*seed``, ``3*seed+1`` and ``3*seed+2`` with
   ``seed = 20260000 + index``.
 * ``scale = 1/sqrt(d)``.
+* Backward cases add dO iid N(0, 1), rounded to bf16, on the stream ``4*seed + 3``.
 * The packed variable-length batch draws its 16 lengths uniformly from [128, 4096] with the
   stream ``seed`` itself, and ``cu_seqlens`` is their int32 exclusive prefix sum.
 
@@ -80,6 +81,11 @@ class Workload:
         else:
             out.update({"layout": "[B,H,N,d]", "batch": self.B, "seq_len": self.N})
         return out
+
+    def make_dout(self):
+        """The upstream gradient dO for a backward case: iid N(0, 1) rounded to bf16, shaped like
+        Q, on the splitmix64 stream ``4*seed + 3``."""
+        return inputs.bf16_normal(4 * self.seed + 3, self.shape(), 1.0)
 
     def make(self, shape=None):
         """(q, k, v) as uint16 bf16 bit arrays, plus cu_seqlens (int32) or None.  K and V have

@@ -130,6 +130,35 @@ ATTN_API int attn_fwd_splitkv_slices(int B, int H, int N, int num_splits);
 ATTN_API size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
 /*
+ * Backward pass (dQ, dK, dV) of the fused forward.  Nothing N x N is read or kept: S and P are
+ * rebuilt tile by tile from the logsumexp the forward saved (CS336 Lecture 5 notes, section 6.2,
+ * "反向传播怎么办"), and the gradients follow from the definition by the chain rule:
+ * dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with D_i = dO_i . O_i, dQ = scale dS K,
+ * dK = scale dS^T Q.  Three kernel launches on `stream`: a row pass (D and lse * log2 e into the
+ * workspace), a dK/dV kernel (one CTA per 128-key tile) and a dQ kernel (one CTA per 128-query
+ * tile); every output element is written once (deterministic, no atomics).
+ * Dense layout only:
+ *   q, k, v, o, dout : bf16 [B, H, N, d] (o is the forward's output, dout the gradient of the loss
+ *                      with respect to it)         lse : fp32 [B, H, N], the forward's lse output
+ *   dq, dk, dv       : bf16 [B, H, N, d] outputs
+ *   causal, scale    : as in the forward call that produced o and lse
+ *   workspace        : caller-owned device buffer of at least attn_bwd_workspace_bytes(B,H,N,d)
+ *                      bytes, 256-byte aligned; contents on return unspecified
+ * Every tensor pointer must be 16-byte aligned (ATTN_ERR_ALIGN) and non-NULL (ATTN_ERR_NULL);
+ * other checks as attn_fwd.  Returns an attn_status.
+ */
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int H, int N, int d, int causal, float scale, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes attn_bwd needs: two fp32 planes of B * H * Npad values (Npad = N rounded up to
+ * 128), each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ */
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * Unfused comparison path (the "standard attention" of the pages: S written to HBM, read back for
  * the softmax, P written to HBM, read back for P V; CS336 GPU/attention notes, "Attention 为什么
  * 容易 memory-bound"; CS336 Lecture 5 notes, section 6.1).  Three kernel launches on `stream`:

@@ -30,6 +30,8 @@ SIGNATURES = {
     "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "attn_fwd_splitkv_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
     "attn_fwd_splitkv_slices": (_I, [_I, _I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "attn_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_fwd_unfused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_fwd_unfused_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_fwd_unfused_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -171,6 +173,41 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
                                     _stream_handle(stream, q.device))
     _check("attn_fwd_splitkv", rc)
     return out, lse
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+             workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Backward pass: gradients (dQ, dK, dV) of the fused forward for the upstream gradient
+    ``dout``, given the forward's ``o`` and ``lse``.  Dense [B, H, N, d] only."""
+    import torch
+    B, H, _, N, d = _check_inputs(q, k, v, None)
+    for name, t in (("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != q.shape or \
+                t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != q.shape[:-1] or \
+            lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 tensor of shape [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        rc = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream_handle(stream, q.device))
+    _check("attn_bwd", rc)
+    return dq, dk, dv
 
 
 def unfused_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

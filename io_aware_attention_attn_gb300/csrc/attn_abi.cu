@@ -9,6 +9,7 @@
 
 #include "attn_gb300.h"
 #include "attn_host.h"
+#include "attn_bwd.h"
 #include "attn_params.h"
 
 namespace attn {
@@ -217,6 +218,63 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
                                                   256 * 256);
   return fwd_impl(q, k, v, o, lse, nullptr, B, H, H, N, d, causal, scale, stream, S, part_o,
                   part_stat);
+}
+
+// Backward workspace: two fp32 planes [B*H][n_pad] (lse * log2(e), then D), each rounded up to
+// 256 bytes.
+static size_t bwd_plane_bytes(int B, int H, int N) {
+  const size_t n_pad = (static_cast<size_t>(N) + kBM - 1) / kBM * kBM;
+  return (static_cast<size_t>(B) * H * n_pad * 4 + 255) / 256 * 256;
+}
+
+extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  return 2 * bwd_plane_bytes(B, H, N);
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int H, int N, int d, int causal, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  bool empty = false;
+  int rc = validate(q, k, v, o, lse, nullptr, B, H, N, d, scale, &empty);
+  if (rc != ATTN_OK || empty) return rc;
+  if (!dout || !dq || !dk || !dv) return ATTN_ERR_NULL;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_ALIGN;
+  const size_t plane = bwd_plane_bytes(B, H, N);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      workspace_bytes < 2 * plane)
+    return ATTN_ERR_WORKSPACE;
+  if ((rc = check_device()) != 0) return rc;
+  BwdParams p{};
+  const uint64_t heads = static_cast<uint64_t>(B) * H;
+  if (encode_rows_map(&p.tm_q, q, d, N, heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_k, k, d, N, heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_v, v, d, N, heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_do, dout, d, N, heads) != CUDA_SUCCESS)
+    return ATTN_ERR_LAUNCH;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  float* lse2 = static_cast<float*>(workspace);
+  float* dd = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plane);
+  p.lse2 = lse2;
+  p.dd = dd;
+  p.status = status_word();
+  if (!p.status) return ATTN_ERR_LAUNCH;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.n_tiles = (N + kBM - 1) / kBM;
+  p.n_pad = p.n_tiles * kBM;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_prep(o, dout, lse, lse2, dd, B * H, N, p.n_pad, d, st);
+  if (e == cudaSuccess)
+    e = (d == 64) ? launch_bwd_d64(p, causal != 0, st) : launch_bwd_d128(p, causal != 0, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 extern "C" int attn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse,

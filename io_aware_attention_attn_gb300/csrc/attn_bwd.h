@@ -1,0 +1,112 @@
+// attn_bwd.h -- launch parameters, shared-memory layouts and launchers of the backward pass.
+//
+// The backward recomputes S and P tile by tile from the logsumexp the forward saved (CS336
+// Lecture 5 notes, section 6.2, "反向传播怎么办") and applies the chain rule of the definition:
+// dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with D_i = dO_i . O_i, dQ = scale dS K,
+// dK = scale dS^T Q.  Three launches:
+//   bwd_prep_kernel         D_i and lse_i * log2(e) per query row, into padded fp32 planes
+//   attn_bwd_dkdv_kernel    one CTA per (head, 128-key tile): dK and dV accumulated in tensor
+//                           memory over the query tiles
+//   attn_bwd_dq_kernel      one CTA per (head, 128-query tile): dQ accumulated in tensor memory
+//                           over the key tiles
+// Every output element is written by exactly one CTA: no atomics, the result is deterministic.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "attn_params.h"
+
+namespace attn {
+
+constexpr int kBwdThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 two column halves
+constexpr int kBwdStages = 2;     // depth of the streamed-tile rings
+
+struct BwdParams {
+  CUtensorMap tm_q;   // 3-D maps over [B*H][N][D] bf16, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  __nv_bfloat16* dq;  // outputs [B, H, N, D] bf16
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* lse2;  // [B*H][n_pad]: lse * log2(e); +inf in rows >= N
+  const float* dd;    // [B*H][n_pad]: rowsum(dO * O); 0 in rows >= N
+  int* status;        // device status word (bounded waits)
+  int B, H, N;
+  int n_tiles;        // ceil(N / 128)
+  int n_pad;          // n_tiles * 128
+  float scale_log2;   // scale * log2(e)
+  float scale;
+};
+
+// dK/dV kernel: K_j and V_j resident; Q_i, dO_i and the per-query vectors (lse2, D) stream
+// through a kBwdStages ring.
+template <int D>
+struct BwdKvLayout {
+  static constexpr int kTile = kBM * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;                    // [kBwdStages]
+  static constexpr int kDO = kQ + kBwdStages * kTile;      // [kBwdStages]
+  static constexpr int kVec = kDO + kBwdStages * kTile;    // [kBwdStages] x (lse2[128], D[128])
+  static constexpr int kBar = kVec + kBwdStages * 1024;
+  enum {
+    bKV = 0,                  // K_j and V_j landed
+    bQF = 1,                  // Q_i, dO_i and vectors landed [kBwdStages]
+    bQE = bQF + kBwdStages,   // stage free                   [kBwdStages]
+    bS = bQE + kBwdStages,    // S^T = K Q^T written
+    bDP,                      // dP^T = V dO^T written
+    bP,                       // P^T (bf16) written over S^T (256 arrivals)
+    bDS,                      // dS^T (bf16) written over dP^T (256 arrivals)
+    bDV,                      // dV += P^T dO completed
+    bDK,                      // dK += dS^T Q completed (and every earlier MMA)
+    bDR,                      // drain after an abort
+    kNumBars
+  };
+  static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kDynBytes = kBytes + 1024;
+};
+
+// dQ kernel: Q_i and dO_i resident; K_j and V_j stream through kBwdStages rings.
+template <int D>
+struct BwdQLayout {
+  static constexpr int kTile = kBM * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTile;
+  static constexpr int kK = kDO + kTile;                   // [kBwdStages]
+  static constexpr int kV = kK + kBwdStages * kTile;       // [kBwdStages]
+  static constexpr int kBar = kV + kBwdStages * kTile;
+  enum {
+    bQ = 0,                   // Q_i and dO_i landed
+    bKF = 1,                  // K stage full [kBwdStages]
+    bKE = bKF + kBwdStages,   // K stage free [kBwdStages]
+    bVF = bKE + kBwdStages,   // V stage full [kBwdStages]
+    bVE = bVF + kBwdStages,   // V stage free [kBwdStages]
+    bS = bVE + kBwdStages,    // S = Q K^T written
+    bSR,                      // S read by every compute thread (256 arrivals)
+    bDP,                      // dP = dO V^T written
+    bDS,                      // dS (bf16) written over dP (256 arrivals)
+    bDQ,                      // dQ += dS K completed (and every earlier MMA)
+    bDR,                      // drain after an abort
+    kNumBars
+  };
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kDynBytes = kBytes + 1024;
+};
+
+static_assert(BwdKvLayout<128>::kDynBytes <= 232448, "dK/dV kernel exceeds 227 KB shared memory");
+static_assert(BwdQLayout<128>::kDynBytes <= 232448, "dQ kernel exceeds 227 KB shared memory");
+
+// Launchers (one translation unit per head dimension for the tile kernels).
+cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, cudaStream_t stream);
+cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, cudaStream_t stream);
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2,
+                            float* dd, int BH, int N, int n_pad, int d, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,591 @@
+// attn_bwd_kernels.cuh -- tcgen05 kernels of the attention backward pass for sm_103a (GB300).
+//
+// Both tile kernels keep one 128-row tile resident, stream the other operand's tiles through
+// TMA-fed shared-memory rings, and rebuild P from the saved logsumexp instead of reading any
+// N x N matrix (CS336 Lecture 5 notes, section 6.2, "反向传播怎么办").
+//
+// Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA issuer (lane 0);
+// warps 2..9 compute.  A compute thread owns one row of the resident tile (its TMEM lane: warp
+// w may access lanes 32*(w%4)..+31) and one half of the streamed tile's 128 columns: warps 2..5
+// take columns 0..63, warps 6..9 columns 64..127.
+//
+// dK/dV kernel (rows = 128 keys of tile j, columns = 128 queries of tile i), per query tile:
+//   S^T  = K_j Q_i^T      (SS MMA into TMEM columns 0..127)
+//   dP^T = V_j dO_i^T     (SS MMA into TMEM columns 128..255)
+//   P^T  = 2^(S^T scale log2e - lse2_i) per element, bf16, written back over the first 32
+//          columns of each half of S^T; dS^T = P^T * (dP^T - D_i), bf16, over dP^T likewise
+//   dV  += P^T dO_i       (TS MMA, A = P^T from TMEM, B = dO_i MN-major; TMEM 256..256+D)
+//   dK  += dS^T Q_i       (TS MMA, A = dS^T from TMEM, B = Q_i MN-major; TMEM 256+D..)
+// dQ kernel (rows = 128 queries of tile i, columns = 128 keys of tile j), per key tile:
+//   S = Q_i K_j^T, dP = dO_i V_j^T (SS), P and dS as above with per-row lse2 and D,
+//   dQ += dS K_j          (TS MMA, B = K_j MN-major; TMEM 256..256+D)
+// Each TS MMA reads its A operand from the columns it was written to, so the next tile's SS MMA
+// into the same columns waits for that TS MMA to complete (tcgen05 MMAs with different
+// accumulators are not ordered).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_bwd.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace bwd {
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// SS product over D/16 K-steps: both operands K-major 128-row tiles (D/64 blocks of 16 KB,
+// 128-byte rows, 32 bytes per K-step of 16 elements).
+template <int D>
+__device__ __forceinline__ void mma_ss_tile(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                            uint32_t idesc) {
+  #pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint64_t off = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+    mma_bf16_ss(d_tmem, a + off, b + off, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// TS product over 128 rows of K: A = 128 bf16 values per TMEM lane, stored as two halves of 64
+// (32 packed columns each) at column offsets 0 and 64; B = a 128-row MN-major tile (16 rows =
+// 2048 bytes per K-step).
+__device__ __forceinline__ void mma_ts_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, bool accumulate) {
+  #pragma unroll
+  for (int k = 0; k < kBN / 16; ++k)
+    mma_bf16_ts(d_tmem, a_tmem + (k >> 2) * 64 + (k & 3) * 8,
+                b + static_cast<uint64_t>(k * (2048 >> 4)), idesc,
+                (accumulate || k > 0) ? 1u : 0u);
+}
+
+// Write one row's half of a D-wide fp32 accumulator (TMEM columns col .. col + D/2 - 1) as bf16,
+// multiplied by `mul`, to dst[0 .. D/2 - 1] (16-byte aligned).
+template <int D>
+__device__ __forceinline__ void store_row_half(uint32_t col, float mul, __nv_bfloat16* dst,
+                                               bool valid) {
+  #pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t v[32];
+    tmem_ld32(col + 32 * c, v);
+    tmem_wait_ld_regs(v);
+    if (valid) {
+      uint4* out = reinterpret_cast<uint4*>(dst + 32 * c);
+      #pragma unroll
+      for (int q = 0; q < 4; ++q)
+        out[q] = make_uint4(pack_bf16x2(u2f(v[8 * q + 0]) * mul, u2f(v[8 * q + 1]) * mul),
+                            pack_bf16x2(u2f(v[8 * q + 2]) * mul, u2f(v[8 * q + 3]) * mul),
+                            pack_bf16x2(u2f(v[8 * q + 4]) * mul, u2f(v[8 * q + 5]) * mul),
+                            pack_bf16x2(u2f(v[8 * q + 6]) * mul, u2f(v[8 * q + 7]) * mul));
+    }
+  }
+}
+
+}  // namespace bwd
+
+// =============================================================================== dK / dV kernel
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using Lay = BwdKvLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_s);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);
+  const WaitCtx wc{reinterpret_cast<volatile int*>(misc + 1), p.status};
+  auto bar = [&](int i) -> uint32_t { return sbase + Lay::kBar + 8u * static_cast<uint32_t>(i); };
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Lay::bKV), 1);
+    for (int s = 0; s < kBwdStages; ++s) {
+      mbar_init(bar(Lay::bQF + s), 1);
+      mbar_init(bar(Lay::bQE + s), 1);
+    }
+    mbar_init(bar(Lay::bS), 1);
+    mbar_init(bar(Lay::bDP), 1);
+    mbar_init(bar(Lay::bP), 8 * 32);
+    mbar_init(bar(Lay::bDS), 8 * 32);
+    mbar_init(bar(Lay::bDV), 1);
+    mbar_init(bar(Lay::bDK), 1);
+    mbar_init(bar(Lay::bDR), 1);
+    fence_barrier_init();
+    misc[1] = 0;
+  }
+
+  // key tile j of head slice z; causal: query tiles j .. n_tiles-1 (the most first), else all
+  const int BH = p.B * p.H;
+  const int L = static_cast<int>(blockIdx.x);
+  int z, j;
+  if constexpr (CAUSAL) {
+    j = L / BH;
+    z = L % BH;
+  } else {  // the key tiles of a head together: its Q and dO tiles stay in L2
+    z = L / p.n_tiles;
+    j = L % p.n_tiles;
+  }
+  const int i0 = CAUSAL ? j : 0;
+  const int n_it = p.n_tiles - i0;
+
+  __syncthreads();
+  if (warp == 1) {
+    tmem_alloc(sbase + Lay::kMisc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  constexpr uint64_t kTileD = static_cast<uint64_t>(Lay::kTile >> 4);
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      const uint64_t keep = l2_policy_evict_last();   // Q, dO: re-read by every key tile
+      const uint64_t once = l2_policy_evict_first();  // K, V: read once
+      mbar_arrive_expect_tx(bar(Lay::bKV), 2 * Lay::kTile);
+      #pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d_hint(sbase + Lay::kK + c * 16384, &p.tm_k, bar(Lay::bKV), c * 64, j * kBN, z,
+                         once);
+        tma_load_3d_hint(sbase + Lay::kV + c * 16384, &p.tm_v, bar(Lay::bKV), c * 64, j * kBN, z,
+                         once);
+      }
+      const float* lse2 = p.lse2 + static_cast<size_t>(z) * p.n_pad;
+      const float* dd = p.dd + static_cast<size_t>(z) * p.n_pad;
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_it; ++t) {
+        const int s = t % kBwdStages;
+        if (t >= kBwdStages &&
+            !(ok = mbar_wait(bar(Lay::bQE + s),
+                             (static_cast<uint32_t>(t / kBwdStages) & 1u) ^ 1u, wc, 0, 1)))
+          break;
+        const int i = i0 + t;
+        mbar_arrive_expect_tx(bar(Lay::bQF + s), 2 * Lay::kTile + 1024);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d_hint(sbase + Lay::kQ + s * Lay::kTile + c * 16384, &p.tm_q,
+                           bar(Lay::bQF + s), c * 64, i * kBM, z, keep);
+          tma_load_3d_hint(sbase + Lay::kDO + s * Lay::kTile + c * 16384, &p.tm_do,
+                           bar(Lay::bQF + s), c * 64, i * kBM, z, keep);
+        }
+        bulk_load_1d(sbase + Lay::kVec + s * 1024, lse2 + i * kBM, 512, bar(Lay::bQF + s));
+        bulk_load_1d(sbase + Lay::kVec + s * 1024 + 512, dd + i * kBM, 512, bar(Lay::bQF + s));
+        ++issued;
+      }
+      if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
+        mbar_wait_drain(bar(Lay::bKV), 0);
+        for (int t = (issued > kBwdStages ? issued - kBwdStages : 0); t < issued; ++t)
+          mbar_wait_drain(bar(Lay::bQF + t % kBwdStages),
+                          static_cast<uint32_t>(t / kBwdStages) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
+    constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
+    const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
+    const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16, 1024);
+    const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);         // K-major use
+    const uint64_t desc_do = sdesc_sw128(sbase + Lay::kDO, 16, 1024);
+    const uint64_t desc_q_mn = sdesc_sw128(sbase + Lay::kQ, 16384, 1024);   // MN-major use
+    const uint64_t desc_do_mn = sdesc_sw128(sbase + Lay::kDO, 16384, 1024);
+    bool ok = mbar_wait_warp(bar(Lay::bKV), 0, wc, 1, 2);
+    for (int t = 0; ok && t < n_it; ++t) {
+      const int s = t % kBwdStages;
+      const uint32_t par = static_cast<uint32_t>(t) & 1u;
+      if (!(ok = mbar_wait_warp(bar(Lay::bQF + s), static_cast<uint32_t>(t / kBwdStages) & 1u,
+                                wc, 1, 3)))
+        break;
+      // S^T_t rewrites the columns P^T_{t-1} was read from: wait for dV_{t-1}
+      if (t > 0 && !(ok = mbar_wait_warp(bar(Lay::bDV), par ^ 1u, wc, 1, 4))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        bwd::mma_ss_tile<D>(tmem + kColS, desc_k, desc_q + s * kTileD, kIdSS);
+        mma_commit(bar(Lay::bS));
+      }
+      __syncwarp();
+      // dP^T_t rewrites the columns dS^T_{t-1} was read from: wait for dK_{t-1}
+      if (t > 0 && !(ok = mbar_wait_warp(bar(Lay::bDK), par ^ 1u, wc, 1, 5))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        bwd::mma_ss_tile<D>(tmem + kColDP, desc_v, desc_do + s * kTileD, kIdSS);
+        mma_commit(bar(Lay::bDP));
+      }
+      __syncwarp();
+      if (!(ok = mbar_wait_warp(bar(Lay::bP), par, wc, 1, 6))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        bwd::mma_ts_tile(tmem + kColDV, tmem + kColS, desc_do_mn + s * kTileD, kIdTS, t > 0);
+        mma_commit(bar(Lay::bDV));
+      }
+      __syncwarp();
+      if (!(ok = mbar_wait_warp(bar(Lay::bDS), par, wc, 1, 7))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        bwd::mma_ts_tile(tmem + kColDK, tmem + kColDP, desc_q_mn + s * kTileD, kIdTS, t > 0);
+        mma_commit(bar(Lay::bDK));
+        mma_commit(bar(Lay::bQE + s));
+      }
+      __syncwarp();
+    }
+    if (!ok) {  // unwinding: wait for every MMA already issued
+      if (lane == 0) mma_commit(bar(Lay::bDR));
+      __syncwarp();
+      mbar_wait_drain(bar(Lay::bDR), 0);
+    }
+  } else {
+    // ================================================================ compute
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;  // key row within the tile (= TMEM lane)
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t col_s = t_lane + kColS + 64 * half;
+    const uint32_t col_dp = t_lane + kColDP + 64 * half;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < n_it; ++t) {
+      const int s = t % kBwdStages;
+      const uint32_t par = static_cast<uint32_t>(t) & 1u;
+      const int i = i0 + t;
+      if (!(ok = mbar_wait_warp(bar(Lay::bQF + s), static_cast<uint32_t>(t / kBwdStages) & 1u,
+                                wc, 2, 8)))
+        break;
+      if (!(ok = mbar_wait_warp(bar(Lay::bS), par, wc, 2, 9))) break;
+      tc_fence_after();
+      const float* vec = reinterpret_cast<const float*>(smem + Lay::kVec + s * 1024) + 64 * half;
+      float pf[64];
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(col_s, u0);
+        tmem_ld32(col_s + 32, u1);
+        tmem_wait_ld_regs(u0);
+        tmem_wait_ld_regs(u1);
+        #pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          pf[c] = bwd::u2f(u0[c]);
+          pf[32 + c] = bwd::u2f(u1[c]);
+        }
+      }
+      #pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l = reinterpret_cast<const float4*>(vec)[c4];
+        pf[4 * c4 + 0] = ex2_approx(fmaf(pf[4 * c4 + 0], sl2, -l.x));
+        pf[4 * c4 + 1] = ex2_approx(fmaf(pf[4 * c4 + 1], sl2, -l.y));
+        pf[4 * c4 + 2] = ex2_approx(fmaf(pf[4 * c4 + 2], sl2, -l.z));
+        pf[4 * c4 + 3] = ex2_approx(fmaf(pf[4 * c4 + 3], sl2, -l.w));
+      }
+      if (CAUSAL && i == j) {  // diagonal tile: query 64*half + c precedes key r when < r
+        #pragma unroll
+        for (int c = 0; c < 64; ++c) pf[c] = (64 * half + c < r) ? 0.f : pf[c];
+      }
+      {
+        uint32_t pk[32];
+        #pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
+        tmem_st32(col_s, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(Lay::bP));
+
+      if (!(ok = mbar_wait_warp(bar(Lay::bDP), par, wc, 2, 10))) break;
+      tc_fence_after();
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(col_dp, u0);
+        tmem_ld32(col_dp + 32, u1);
+        tmem_wait_ld_regs(u0);
+        tmem_wait_ld_regs(u1);
+        const float* dvec = vec + 128;
+        uint32_t pk[32];
+        #pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dl = reinterpret_cast<const float4*>(dvec)[c4];
+          const int c = 4 * c4;
+          pk[2 * c4] = pack_bf16x2(pf[c] * (bwd::u2f(u0[c]) - dl.x), pf[c + 1] * (bwd::u2f(u0[c + 1]) - dl.y));
+          pk[2 * c4 + 1] =
+              pack_bf16x2(pf[c + 2] * (bwd::u2f(u0[c + 2]) - dl.z), pf[c + 3] * (bwd::u2f(u0[c + 3]) - dl.w));
+        }
+        #pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dl = reinterpret_cast<const float4*>(dvec)[8 + c4];
+          const int c = 4 * c4;
+          pk[16 + 2 * c4] = pack_bf16x2(pf[32 + c] * (bwd::u2f(u1[c]) - dl.x),
+                                        pf[32 + c + 1] * (bwd::u2f(u1[c + 1]) - dl.y));
+          pk[16 + 2 * c4 + 1] = pack_bf16x2(pf[32 + c + 2] * (bwd::u2f(u1[c + 2]) - dl.z),
+                                            pf[32 + c + 3] * (bwd::u2f(u1[c + 3]) - dl.w));
+        }
+        tmem_st32(col_dp, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(Lay::bDS));
+    }
+    // epilogue: the last dK commit covers every MMA of the CTA
+    if (ok) ok = mbar_wait_warp(bar(Lay::bDK), static_cast<uint32_t>(n_it - 1) & 1u, wc, 2, 11);
+    if (ok) {
+      tc_fence_after();
+      const int key = j * kBN + r;
+      const bool valid = key < p.N;
+      const size_t row = static_cast<size_t>(z) * p.N + (valid ? key : 0);
+      bwd::store_row_half<D>(t_lane + kColDV + half * (D / 2), 1.f, p.dv + row * D + half * (D / 2),
+                             valid);
+      bwd::store_row_half<D>(t_lane + kColDK + half * (D / 2), p.scale,
+                             p.dk + row * D + half * (D / 2), valid);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =================================================================================== dQ kernel
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using Lay = BwdQLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_s);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);
+  const WaitCtx wc{reinterpret_cast<volatile int*>(misc + 1), p.status};
+  auto bar = [&](int i) -> uint32_t { return sbase + Lay::kBar + 8u * static_cast<uint32_t>(i); };
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Lay::bQ), 1);
+    for (int s = 0; s < kBwdStages; ++s) {
+      mbar_init(bar(Lay::bKF + s), 1);
+      mbar_init(bar(Lay::bKE + s), 1);
+      mbar_init(bar(Lay::bVF + s), 1);
+      mbar_init(bar(Lay::bVE + s), 1);
+    }
+    mbar_init(bar(Lay::bS), 1);
+    mbar_init(bar(Lay::bSR), 8 * 32);
+    mbar_init(bar(Lay::bDP), 1);
+    mbar_init(bar(Lay::bDS), 8 * 32);
+    mbar_init(bar(Lay::bDQ), 1);
+    mbar_init(bar(Lay::bDR), 1);
+    fence_barrier_init();
+    misc[1] = 0;
+  }
+
+  // query tile i of head slice z; causal: key tiles 0..i (the heaviest tiles first), else all
+  const int BH = p.B * p.H;
+  const int L = static_cast<int>(blockIdx.x);
+  int z, i;
+  if constexpr (CAUSAL) {
+    i = p.n_tiles - 1 - L / BH;
+    z = L % BH;
+  } else {  // the query tiles of a head together: its K and V tiles stay in L2
+    z = L / p.n_tiles;
+    i = L % p.n_tiles;
+  }
+  const int n_kv = CAUSAL ? i + 1 : p.n_tiles;
+
+  __syncthreads();
+  if (warp == 1) {
+    tmem_alloc(sbase + Lay::kMisc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  constexpr uint64_t kTileD = static_cast<uint64_t>(Lay::kTile >> 4);
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      const uint64_t keep = l2_policy_evict_last();   // K, V: re-read by every query tile
+      const uint64_t once = l2_policy_evict_first();  // Q, dO: read once
+      mbar_arrive_expect_tx(bar(Lay::bQ), 2 * Lay::kTile);
+      #pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d_hint(sbase + Lay::kQ + c * 16384, &p.tm_q, bar(Lay::bQ), c * 64, i * kBM, z,
+                         once);
+        tma_load_3d_hint(sbase + Lay::kDO + c * 16384, &p.tm_do, bar(Lay::bQ), c * 64, i * kBM,
+                         z, once);
+      }
+      int nk = 0, nv = 0;
+      bool ok = true;
+      for (int jj = 0; jj < n_kv; ++jj) {
+        const int s = jj % kBwdStages;
+        const uint32_t free_par = (static_cast<uint32_t>(jj / kBwdStages) & 1u) ^ 1u;
+        if (jj >= kBwdStages && !(ok = mbar_wait(bar(Lay::bKE + s), free_par, wc, 0, 1))) break;
+        mbar_arrive_expect_tx(bar(Lay::bKF + s), Lay::kTile);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sbase + Lay::kK + s * Lay::kTile + c * 16384, &p.tm_k,
+                           bar(Lay::bKF + s), c * 64, jj * kBN, z, keep);
+        ++nk;
+        if (jj >= kBwdStages && !(ok = mbar_wait(bar(Lay::bVE + s), free_par, wc, 0, 2))) break;
+        mbar_arrive_expect_tx(bar(Lay::bVF + s), Lay::kTile);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sbase + Lay::kV + s * Lay::kTile + c * 16384, &p.tm_v,
+                           bar(Lay::bVF + s), c * 64, jj * kBN, z, keep);
+        ++nv;
+      }
+      if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
+        mbar_wait_drain(bar(Lay::bQ), 0);
+        for (int t = (nk > kBwdStages ? nk - kBwdStages : 0); t < nk; ++t)
+          mbar_wait_drain(bar(Lay::bKF + t % kBwdStages),
+                          static_cast<uint32_t>(t / kBwdStages) & 1u);
+        for (int t = (nv > kBwdStages ? nv - kBwdStages : 0); t < nv; ++t)
+          mbar_wait_drain(bar(Lay::bVF + t % kBwdStages),
+                          static_cast<uint32_t>(t / kBwdStages) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
+    constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
+    const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);
+    const uint64_t desc_do = sdesc_sw128(sbase + Lay::kDO, 16, 1024);
+    const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);          // K-major use
+    const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16, 1024);
+    const uint64_t desc_k_mn = sdesc_sw128(sbase + Lay::kK, 16384, 1024);    // MN-major use
+    bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 2);
+    for (int jj = 0; ok && jj < n_kv; ++jj) {
+      const int s = jj % kBwdStages;
+      const uint32_t par = static_cast<uint32_t>(jj) & 1u;
+      const uint32_t full_par = static_cast<uint32_t>(jj / kBwdStages) & 1u;
+      if (!(ok = mbar_wait_warp(bar(Lay::bKF + s), full_par, wc, 1, 3))) break;
+      // S_jj rewrites columns the compute threads read S_{jj-1} from
+      if (jj > 0 && !(ok = mbar_wait_warp(bar(Lay::bSR), par ^ 1u, wc, 1, 4))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        bwd::mma_ss_tile<D>(tmem + kColS, desc_q, desc_k + s * kTileD, kIdSS);
+        mma_commit(bar(Lay::bS));
+      }
+      __syncwarp();
+      if (!(ok = mbar_wait_warp(bar(Lay::bVF + s), full_par, wc, 1, 5))) break;
+      // dP_jj rewrites the columns dS_{jj-1} was read from: wait for dQ_{jj-1}
+      if (jj > 0 && !(ok = mbar_wait_warp(bar(Lay::bDQ), par ^ 1u, wc, 1, 6))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        bwd::mma_ss_tile<D>(tmem + kColDP, desc_do, desc_v + s * kTileD, kIdSS);
+        mma_commit(bar(Lay::bDP));
+        mma_commit(bar(Lay::bVE + s));
+      }
+      __syncwarp();
+      if (!(ok = mbar_wait_warp(bar(Lay::bDS), par, wc, 1, 7))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        bwd::mma_ts_tile(tmem + kColDQ, tmem + kColDP, desc_k_mn + s * kTileD, kIdTS, jj > 0);
+        mma_commit(bar(Lay::bDQ));
+        mma_commit(bar(Lay::bKE + s));
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      if (lane == 0) mma_commit(bar(Lay::bDR));
+      __syncwarp();
+      mbar_wait_drain(bar(Lay::bDR), 0);
+    }
+  } else {
+    // ================================================================ compute
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;  // query row within the tile (= TMEM lane)
+    const int row = i * kBM + r;        // query row within the sequence (padded rows < n_pad)
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t col_s = t_lane + kColS + 64 * half;
+    const uint32_t col_dp = t_lane + kColDP + 64 * half;
+    const float sl2 = p.scale_log2;
+    const float lse2 = p.lse2[static_cast<size_t>(z) * p.n_pad + row];
+    const float dd = p.dd[static_cast<size_t>(z) * p.n_pad + row];
+    bool ok = true;
+    for (int jj = 0; jj < n_kv; ++jj) {
+      const uint32_t par = static_cast<uint32_t>(jj) & 1u;
+      if (!(ok = mbar_wait_warp(bar(Lay::bS), par, wc, 2, 8))) break;
+      tc_fence_after();
+      float pf[64];
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(col_s, u0);
+        tmem_ld32(col_s + 32, u1);
+        tmem_wait_ld_regs(u0);
+        tmem_wait_ld_regs(u1);
+        #pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          pf[c] = bwd::u2f(u0[c]);
+          pf[32 + c] = bwd::u2f(u1[c]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(Lay::bSR));  // S columns may be rewritten
+      #pragma unroll
+      for (int c = 0; c < 64; ++c) pf[c] = ex2_approx(fmaf(pf[c], sl2, -lse2));
+      // keys past the end of the sequence, and (diagonal tile) keys after the query, get P = 0
+      const int key0 = jj * kBN + 64 * half;
+      if ((CAUSAL && jj == i) || key0 + 64 > p.N) {
+        const int lim = CAUSAL ? min(p.N - key0, row - key0 + 1) : (p.N - key0);
+        #pragma unroll
+        for (int c = 0; c < 64; ++c) pf[c] = (c < lim) ? pf[c] : 0.f;
+      }
+      if (!(ok = mbar_wait_warp(bar(Lay::bDP), par, wc, 2, 9))) break;
+      tc_fence_after();
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(col_dp, u0);
+        tmem_ld32(col_dp + 32, u1);
+        tmem_wait_ld_regs(u0);
+        tmem_wait_ld_regs(u1);
+        uint32_t pk[32];
+        #pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack_bf16x2(pf[2 * c] * (bwd::u2f(u0[2 * c]) - dd),
+                              pf[2 * c + 1] * (bwd::u2f(u0[2 * c + 1]) - dd));
+        #pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[16 + c] = pack_bf16x2(pf[32 + 2 * c] * (bwd::u2f(u1[2 * c]) - dd),
+                                   pf[32 + 2 * c + 1] * (bwd::u2f(u1[2 * c + 1]) - dd));
+        tmem_st32(col_dp, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(Lay::bDS));
+    }
+    if (ok) ok = mbar_wait_warp(bar(Lay::bDQ), static_cast<uint32_t>(n_kv - 1) & 1u, wc, 2, 10);
+    if (ok) {
+      tc_fence_after();
+      const bool valid = row < p.N;
+      const size_t grow = static_cast<size_t>(z) * p.N + (valid ? row : 0);
+      bwd::store_row_half<D>(t_lane + kColDQ + half * (D / 2), p.scale,
+                             p.dq + grow * D + half * (D / 2), valid);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn

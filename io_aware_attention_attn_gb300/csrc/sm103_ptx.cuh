@@ -143,6 +143,17 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Untiled bulk copy global -> shared of `bytes` bytes (both addresses 16-byte aligned, bytes a
+// multiple of 16), completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));

@@ -43,3 +43,40 @@ def check(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np
     assert err.mean() <= O_MEAN_ABS, f"{what}: mean abs error {err.mean()}; {stats}"
     assert lerr.max() <= LSE_ABS, f"{what}: LSE error {lerr.max()}; {stats}"
     return stats
+
+
+# ----------------------------------------------------------------------------- backward
+# Tolerance of the backward, derived from its arithmetic.  Each gradient entry is a sum of
+# products (dV_jc = sum_i P_ij dO_ic; dK_jc = scale sum_i dS_ij Q_ic; dQ_ic = scale sum_j dS_ij
+# K_jc) whose first factor the tensor cores take in bf16 (relative rounding <= 2^-9), with
+# dS = P (dP - D) where D comes from the bf16-rounded forward output (|error| <= 2^-9 sum |dO O|).
+# Bounding every term's error by its magnitude gives |error| <= c * A with the "absolute product"
+#   A(dV) = |P|^T |dO|,   A(dK) = scale W^T |Q|,   A(dQ) = scale W |K|,
+#   W = P * (|dP - D| + sum_c |dO_c O_c|),
+# and c = 2^-9 per rounding; the test allows c = 2^-7 on top of the bf16 rounding of the output
+# itself (half a bf16 spacing), and a mean error of at most 2^-9 mean(A).
+GRAD_C = 2.0 ** -7
+GRAD_MEAN_C = 2.0 ** -9
+
+
+def grad_bounds(q, k, v, do, causal, scale):
+    """Absolute products A(dQ), A(dK), A(dV) of one head ([L, d] float64 arrays)."""
+    from oracle import attention as orc
+    p = orc.probabilities(q, k, causal, scale)
+    o = p @ v
+    dd = np.sum(do * o, axis=1, keepdims=True)
+    dabs = np.sum(np.abs(do * o), axis=1, keepdims=True)
+    w = p * (np.abs(do @ v.T - dd) + dabs)
+    return scale * (w @ np.abs(k)), scale * (w.T @ np.abs(q)), p.T @ np.abs(do)
+
+
+def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, bound: np.ndarray, what: str = "") -> dict:
+    assert g_gpu.shape == g_ref.shape == bound.shape, what
+    assert np.isfinite(g_gpu).all(), f"{what}: non-finite gradient"
+    err = np.abs(g_gpu - g_ref)
+    tol = acc.bf16_half_ulp(g_ref) + GRAD_C * bound
+    stats = {"max_abs": float(err.max()), "max_err_over_tol": float((err / tol).max()),
+             "mean_abs": float(err.mean()), "mean_bound": float(bound.mean()), "n": int(err.size)}
+    assert (err <= tol).all(), f"{what}: {int((err > tol).sum())} entries over tolerance; {stats}"
+    assert err.mean() <= GRAD_MEAN_C * bound.mean(), f"{what}: mean error; {stats}"
+    return stats

@@ -152,3 +152,33 @@ def test_splitkv_validation(lib):
     assert f(None, A, A, A, A, 1, 2, 8192, 128, 0, 0.1, 4, A, big, None) == -1
     assert f(A, A, A, A, A, -1, 2, 8192, 128, 0, 0.1, 4, A, big, None) == -3
     assert f(A, A, A, A, A, 0, 2, 8192, 128, 0, 0.1, 4, None, 0, None) == 0
+
+
+def test_bwd_workspace_bytes(lib):
+    f = lib.attn_bwd_workspace_bytes
+    assert f(2, 32, 4096, 128) == 2 * 2 * 32 * 4096 * 4
+    assert f(1, 1, 100, 64) == 2 * 512           # 128 padded rows x 4 bytes, per plane
+    assert f(1, 3, 129, 64) == 2 * 3 * 256 * 4
+    assert f(1, 1, 100, 96) == 0 and f(0, 1, 100, 64) == 0 and f(1, 1, 0, 64) == 0
+
+
+def test_bwd_validation(lib):
+    f = lib.attn_bwd
+    A = ALIGNED
+    big = 1 << 30
+
+    def call_bwd(**kw):
+        a = dict(q=A, k=A, v=A, o=A, lse=A, do=A, dq=A, dk=A, dv=A, B=1, H=2, N=300, d=128,
+                 causal=1, scale=0.1, ws=A, ws_bytes=big)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
+                 a["B"], a["H"], a["N"], a["d"], a["causal"], a["scale"], a["ws"], a["ws_bytes"],
+                 None)
+
+    assert call_bwd(d=96) == -2
+    assert call_bwd(B=-1) == -3
+    assert call_bwd(do=None) == -1 and call_bwd(dk=None) == -1 and call_bwd(o=None) == -1
+    assert call_bwd(dv=A + 4) == -4 and call_bwd(do=A + 2) == -4 and call_bwd(lse=A + 4) == -4
+    assert call_bwd(scale=float("nan")) == -7
+    assert call_bwd(ws=None) == -8 and call_bwd(ws=A + 16) == -8 and call_bwd(ws_bytes=100) == -8
+    assert call_bwd(N=0) == 0 and call_bwd(H=0, dq=None) == 0

@@ -1,0 +1,121 @@
+"""GPU parity of the backward pass (attn_bwd) against the float64 backward oracle.
+
+The kernel receives the forward's outputs as inputs.  Most cases give it the oracle's O rounded
+to bf16 and its LSE in fp32, so the comparison isolates the backward; one case chains the fused
+forward into the backward.  The tolerance is derived from the arithmetic in parity_util.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gen import configs
+from io_aware_attention_attn_gb300 import attn
+from oracle import attention as orc
+from oracle import backward as bwd
+
+from parity_util import check_grad, grad_bounds, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from io_aware_attention_attn_gb300 import build
+    build.build()
+    yield
+    assert attn.last_device_error() == 0
+
+
+def f64_to_bf16_dev(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).cuda()
+
+
+def make_case(w):
+    """Inputs of a backward case: q, k, v and dO (bits) plus the oracle's gradients, O, LSE."""
+    q, k, v, _ = w.make()
+    do = w.make_dout()
+    ref = bwd.attention_bwd_dense(q, k, v, do, w.causal, w.scale)
+    return q, k, v, do, ref
+
+
+def run_bwd(q, k, v, do, o, lse, causal, scale):
+    dq, dk, dv = attn.attn_bwd(to_dev(q), to_dev(k), to_dev(v), o, lse, to_dev(do),
+                               causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return to_f64(dq), to_f64(dk), to_f64(dv)
+
+
+def check_all(q, k, v, do, grads, ref, causal, scale, what, heads=None):
+    dq, dk, dv = grads
+    B, H = q.shape[:2]
+    heads = heads or [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads:
+        qf, kf, vf, dof = (orc.bf16_bits_to_f64(x[b, h]) for x in (q, k, v, do))
+        aq, ak, av = grad_bounds(qf, kf, vf, dof, causal, scale)
+        check_grad(dq[b, h], ref[0][b, h], aq, f"{what} dQ ({b},{h})")
+        check_grad(dk[b, h], ref[1][b, h], ak, f"{what} dK ({b},{h})")
+        check_grad(dv[b, h], ref[2][b, h], av, f"{what} dV ({b},{h})")
+
+
+@pytest.mark.parametrize("seed,B,H,N,d,causal", [
+    (701, 1, 2, 256, 128, False), (702, 1, 2, 256, 128, True),
+    (703, 1, 2, 300, 128, True),      # ragged last tile
+    (704, 2, 1, 129, 64, True),       # a one-row tail tile
+    (705, 1, 3, 777, 64, False),
+    (706, 1, 2, 1000, 128, True),
+    (707, 1, 1, 1, 64, False),        # one key: dV = dO, dQ = dK = 0
+    (708, 1, 2, 512, 128, False),
+])
+def test_bwd_dense(seed, B, H, N, d, causal):
+    w = configs.custom(seed, B, H, N, d, causal)
+    q, k, v, do, ref = make_case(w)
+    o = f64_to_bf16_dev(ref[3])
+    lse = torch.from_numpy(ref[4].astype(np.float32)).cuda()
+    grads = run_bwd(q, k, v, do, o, lse, causal, w.scale)
+    check_all(q, k, v, do, grads, ref, causal, w.scale, w.name)
+
+
+def test_bwd_single_key_closed_form():
+    w = configs.custom(709, 1, 1, 1, 128, True)
+    q, k, v, do, ref = make_case(w)
+    o = f64_to_bf16_dev(ref[3])
+    lse = torch.from_numpy(ref[4].astype(np.float32)).cuda()
+    dq, dk, dv = run_bwd(q, k, v, do, o, lse, True, w.scale)
+    assert np.array_equal(dv, orc.bf16_bits_to_f64(do))
+    assert np.all(np.abs(dq) < 1e-4) and np.all(np.abs(dk) < 1e-4)
+
+
+def test_bwd_after_fused_forward():
+    # the fused forward's own O and LSE feed the backward (the training use)
+    w = configs.custom(710, 1, 2, 640, 128, True, sigma_qk=1.5)
+    q, k, v, do, ref = make_case(w)
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True, scale=w.scale)
+    grads = run_bwd(q, k, v, do, o, lse, True, w.scale)
+    check_all(q, k, v, do, grads, ref, True, w.scale, "fwd->bwd")
+
+
+def test_bwd_deterministic():
+    w = configs.custom(711, 1, 2, 384, 64, False)
+    q, k, v, do, ref = make_case(w)
+    o = f64_to_bf16_dev(ref[3])
+    lse = torch.from_numpy(ref[4].astype(np.float32)).cuda()
+    a = run_bwd(q, k, v, do, o, lse, False, w.scale)
+    b = run_bwd(q, k, v, do, o, lse, False, w.scale)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_full_size_sampled_heads(causal):
+    # the headline shape (B=2, H=32, N=4096, d=128); three heads compared in full
+    w = configs.custom(712, 2, 32, 4096, 128, causal)
+    q, k, v, _ = w.make()
+    do = w.make_dout()
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal, scale=w.scale)
+    grads = run_bwd(q, k, v, do, o, lse, causal, w.scale)
+    heads = [(0, 0), (1, 17), (1, 31)]
+    ref = bwd.attention_bwd_dense(q, k, v, do, causal, w.scale, heads=heads)
+    check_all(q, k, v, do, grads, ref, causal, w.scale, w.name, heads=heads)
