@@ -386,6 +386,46 @@ def run_ours(args, w, rank, world, dist):
                    "speedup": ms_one / ms_auto, "launches_per_step": 2 if chosen > 1 else 1}
         del sq, sk, sv, so, sl, sws
 
+    # ---- backward pass on the same shape (non-causal and causal): dQ, dK, dV from the
+    # forward's O and LSE and a random upstream gradient
+    backward = None
+    if not args.no_extras:
+        backward = {}
+        dout = to_dev(w.make_dout())
+        bws = torch.empty(max(attn.bwd_workspace_bytes(w.B, w.H, w.N, w.d), 1),
+                          dtype=torch.uint8, device=dev)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for causal in (False, True):
+            fo, fl = attn.attn_fwd(q, k, v, causal=causal, scale=w.scale)
+
+            def bwd_step():
+                attn.attn_bwd(q, k, v, fo, fl, dout, causal=causal, scale=w.scale, workspace=bws,
+                              dq=gq, dk=gk, dv=gv)
+
+            for _ in range(3):
+                bwd_step()
+            barrier()
+            evs = []
+            for _ in range(30):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                bwd_step()
+                e1.record(stream)
+                evs.append((e0, e1))
+            barrier()
+            b_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+            b_flops = acc.attention_bwd_flops(w.H, [w.N] * w.B, w.d, causal)
+            backward["causal" if causal else "non_causal"] = {
+                "ms": b_ms, "tflops": b_flops / (b_ms * 1e-3) / 1e12,
+                "frac_of_peak": b_flops / (b_ms * 1e-3) / 1e12 / peak,
+                "flops_counted": "2.5x forward (5 matmuls); the kernels execute 7",
+                "launches_per_step": 3}
+            del fo, fl
+        backward["workload"] = w.name
+        del dout, bws, gq, gk, gv
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
@@ -404,7 +444,7 @@ def run_ours(args, w, rank, world, dist):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "unfused": unfused,
-            "gqa": gqa, "splitkv": splitkv,
+            "gqa": gqa, "splitkv": splitkv, "backward": backward,
             "clocks": clock_info, "gpu_launches": args.steps,
             "kernel_ms_median": statistics.median(per),
         }
@@ -423,7 +463,7 @@ def main():
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the grouped-query and split-KV measurements")
+                    help="skip the grouped-query, split-KV and backward measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -49,6 +49,18 @@ def attention_flops(heads: int, lengths, d: int, causal: bool) -> float:
     return total
 
 
+def attention_bwd_flops(heads: int, lengths, d: int, causal: bool) -> float:
+    """Backward FLOP count: five L x L x d matmuls per head (S recomputed, dP = dO V^T,
+    dV = P^T dO, dQ = dS K, dK = dS^T Q), i.e. 2.5x the forward count, halved for causal."""
+    return 2.5 * attention_flops(heads, lengths, d, causal)
+
+
+def attention_bwd_ideal_bytes(heads: int, total_tokens: int, d: int) -> int:
+    """Backward minimum: read Q, K, V, O, dO once and write dQ, dK, dV once (bf16), read the
+    lse (fp32)."""
+    return heads * total_tokens * (8 * d * 2 + 4)
+
+
 def attention_exact_flops(heads: int, lengths, d: int, causal: bool) -> float:
     """4 d FLOPs per visible (query, key) pair (the causal diagonal counted exactly)."""
     return float(sum(4 * heads * visible_pairs(int(L), causal) * d for L in lengths))
