@@ -17,10 +17,11 @@ Readings (the pages give the format and the idea of per-tile scales, not an algo
   2^8 x 1.75 = 448, as the pages state, and the smallest positive value is 2^-9.
 * a tile is 128 consecutive rows of one head (all d columns), matching the kernel's tiles; its
   scale is amax / 448 in fp32 (1 when the tile is all zero), so the largest magnitude maps to 448;
-* codes are round-to-nearest-even of x / scale, saturating at +-448.  Because a floating-point
-  division decides an integer code, the decision is taken in the kernel's precision: fp32
-  ``amax / 448`` and fp32 ``x / scale`` (IEEE, correctly rounded), then the exact RNE of that
-  fp32 value to E4M3;
+* codes are round-to-nearest-even of x / scale, saturating at +-448; the sign bit is the
+  input's, so a negative value that rounds to zero is the code of -0 (0x80), as IEEE rounding
+  gives.  Because a floating-point division decides an integer code, the decision is taken in
+  the kernel's precision: fp32 ``amax / 448`` and fp32 ``x / scale`` (IEEE, correctly rounded),
+  then the exact RNE of that fp32 value to E4M3;
 * the attention of the FP8 path is the plain definition applied to the dequantized inputs
   ``code value x tile scale`` (so the oracle's output carries the inputs' quantization and the
   comparison measures what the kernel adds: the E4M3 rounding of the probabilities and fp32
@@ -67,8 +68,8 @@ def e4m3_encode(x) -> np.ndarray:
     even_lo = (_POS_CODES[lo] & 1) == 0
     pick_hi = (dhi < dlo) | ((dhi == dlo) & ~even_lo & (hi != lo))
     code = np.where(pick_hi, _POS_CODES[hi], _POS_CODES[lo]).astype(np.uint8)
-    neg = (x < 0) & (code != 0)
-    return np.where(neg, code | 0x80, code).astype(np.uint8)
+    # the sign bit follows the input's sign, also when the magnitude rounds to zero (-0)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
 
 
 def quantize_tiles(x_bits: np.ndarray):
