@@ -159,6 +159,34 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * Per-tile E4M3 quantization (the FP8 format of CS336 Lecture 5 notes, section 3.1: 1 sign,
+ * 4 exponent, 3 mantissa bits, largest magnitude 448; per-tile scaling).  For every tile of 128
+ * rows of a head of the bf16 tensor x [B, H, N, d] (d = 64 or 128):
+ *   scale = amax / 448 in fp32 (1 for an all-zero tile), written to scales[(b*H + h)*T + t]
+ *   (T = ceil(N/128)); code = E4M3 round-to-nearest-even of x / scale (fp32 IEEE division),
+ *   saturating at +-448, the sign bit kept for values that round to zero.
+ *   transpose = 0: codes [B, H, N, d] (N*d bytes per head)
+ *   transpose = 1: codes [B, H, d, Npad] with Npad = 128*T, padding codes 0 (the V operand of
+ *                  attn_fwd_fp8)
+ * x and codes must be 16-byte aligned, scales 4-byte aligned.  Returns an attn_status.
+ */
+ATTN_API int attn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N,
+                               int d, int transpose, void* stream);
+
+/*
+ * FP8 fused forward (FlashAttention-3's FP8 path, CS336 Lecture 5 notes, section 6.3), head dim
+ * 128, dense layout.  Inputs are E4M3 codes with per-tile fp32 scales as attn_quantize_fp8
+ * writes them: q8, k8 [B, H, N, 128] (transpose = 0), vt8 [B, H, 128, Npad] (transpose = 1); the
+ * value of an input element is code x its tile's scale.  S = Q K^T runs on kind::f8f6f4 tensor
+ * cores; the probabilities enter P V as E4M3 codes of P * 256 * sv_j / max(sv) (V's tile scales
+ * folded in); O (bf16) and lse (fp32, natural log of the scaled scores' normaliser) as attn_fwd.
+ * d other than 128: ATTN_ERR_HEAD_DIM.  Returns an attn_status.
+ */
+ATTN_API int attn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,
+                          const void* vt8, const float* sv, void* o, float* lse, int B, int H,
+                          int N, int d, int causal, float scale, void* stream);
+
+/*
  * Unfused comparison path (the "standard attention" of the pages: S written to HBM, read back for
  * the softmax, P written to HBM, read back for P V; CS336 GPU/attention notes, "Attention 为什么
  * 容易 memory-bound"; CS336 Lecture 5 notes, section 6.1).  Three kernel launches on `stream`:

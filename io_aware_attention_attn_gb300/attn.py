@@ -32,6 +32,8 @@ SIGNATURES = {
     "attn_fwd_splitkv_slices": (_I, [_I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "attn_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_unfused": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_fwd_unfused_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_fwd_unfused_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -208,6 +210,51 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
                             _stream_handle(stream, q.device))
     _check("attn_bwd", rc)
     return dq, dk, dv
+
+
+def quantize_fp8(x, transpose: bool = False, stream=None):
+    """Per-tile E4M3 quantization of a dense bf16 tensor [B, H, N, d].  Returns (codes uint8,
+    scales fp32 [B, H, ceil(N/128)]); codes are [B, H, N, d], or [B, H, d, Npad] when
+    ``transpose`` (the V operand of attn_fwd_fp8)."""
+    import torch
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.dim() != 4:
+        raise ValueError("x must be a contiguous [B, H, N, d] bf16 CUDA tensor")
+    B, H, N, d = x.shape
+    T = -(-N // 128)
+    shape = (B, H, d, T * 128) if transpose else (B, H, N, d)
+    codes = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((B, H, T), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().attn_quantize_fp8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), B, H, N,
+                                     d, int(bool(transpose)), _stream_handle(stream, x.device))
+    _check("attn_quantize_fp8", rc)
+    return codes, scales
+
+
+def attn_fwd_fp8(q8, sq, k8, sk, vt8, sv, causal: bool = False, scale: float | None = None,
+                 out=None, lse=None, stream=None):
+    """FP8 fused forward on quantized inputs (see quantize_fp8).  Returns (O bf16, LSE fp32)."""
+    import torch
+    if q8.dtype != torch.uint8 or q8.dim() != 4 or not q8.is_contiguous():
+        raise ValueError("q8 must be contiguous [B, H, N, 128] uint8 codes")
+    B, H, N, d = q8.shape
+    T = -(-N // 128)
+    if k8.shape != q8.shape or vt8.shape != (B, H, d, T * 128) or \
+            sq.shape != (B, H, T) or sk.shape != (B, H, T) or sv.shape != (B, H, T):
+        raise ValueError("k8, vt8 and the scales must match q8 (vt8 is [B, H, d, Npad])")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    with torch.cuda.device(q8.device):
+        rc = lib().attn_fwd_fp8(q8.data_ptr(), sq.data_ptr(), k8.data_ptr(), sk.data_ptr(),
+                                vt8.data_ptr(), sv.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                B, H, N, d, int(bool(causal)), float(scale),
+                                _stream_handle(stream, q8.device))
+    _check("attn_fwd_fp8", rc)
+    return out, lse
 
 
 def unfused_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

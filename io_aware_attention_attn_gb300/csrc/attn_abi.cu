@@ -10,6 +10,7 @@
 #include "attn_gb300.h"
 #include "attn_host.h"
 #include "attn_bwd.h"
+#include "attn_fp8.h"
 #include "attn_params.h"
 
 namespace attn {
@@ -63,6 +64,20 @@ int encode_f32_rows_map(CUtensorMap* map, const void* base, uint64_t cols, uint6
   const cuuint32_t box[3] = {32, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// One-byte codes [heads][rows][inner], box 128 x 128 with the 128-byte swizzle.
+int encode_u8_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                  uint64_t heads) {
+  auto fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[3] = {inner, rows, heads};
+  const cuuint64_t strides[2] = {inner, inner * rows};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
@@ -274,6 +289,64 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   cudaError_t e = launch_bwd_prep(o, dout, lse, lse2, dd, B * H, N, p.n_pad, d, st);
   if (e == cudaSuccess)
     e = (d == 64) ? launch_bwd_d64(p, causal != 0, st) : launch_bwd_d128(p, causal != 0, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N,
+                                 int d, int transpose, void* stream) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (d != 64 && d != 128) return ATTN_ERR_HEAD_DIM;
+  if (!x || !codes || !scales) return ATTN_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return ATTN_ERR_ALIGN;
+  const long long tiles = (static_cast<long long>(N) + kBM - 1) / kBM;
+  if (tiles * B * H > INT_MAX) return ATTN_ERR_SHAPE;
+  int rc = check_device();
+  if (rc != 0) return rc;
+  const cudaError_t e = launch_quantize_fp8(x, codes, scales, B * H, N, d, transpose != 0,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,
+                            const void* vt8, const float* sv, void* o, float* lse, int B, int H,
+                            int N, int d, int causal, float scale, void* stream) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (d != 128) return ATTN_ERR_HEAD_DIM;
+  if (!q8 || !sq || !k8 || !sk || !vt8 || !sv || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned16(lse) ||
+      ((reinterpret_cast<uintptr_t>(sq) | reinterpret_cast<uintptr_t>(sk) |
+        reinterpret_cast<uintptr_t>(sv)) & 3u))
+    return ATTN_ERR_ALIGN;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SCALE;
+  const long long pairs = (static_cast<long long>(N) + 2 * kBM - 1) / (2 * kBM);
+  if (pairs * B * H > INT_MAX) return ATTN_ERR_SHAPE;
+  int rc = check_device();
+  if (rc != 0) return rc;
+  Fp8Params p{};
+  const uint64_t heads = static_cast<uint64_t>(B) * H;
+  const int n_tiles = (N + kBM - 1) / kBM;
+  if (encode_u8_map(&p.tm_q, q8, 128, N, heads) != CUDA_SUCCESS ||
+      encode_u8_map(&p.tm_k, k8, 128, N, heads) != CUDA_SUCCESS ||
+      encode_u8_map(&p.tm_vt, vt8, static_cast<uint64_t>(n_tiles) * kBM, 128, heads) !=
+          CUDA_SUCCESS)
+    return ATTN_ERR_LAUNCH;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.status = status_word();
+  if (!p.status) return ATTN_ERR_LAUNCH;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.n_tiles = n_tiles;
+  p.n_qt = static_cast<int>(pairs);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e = launch_fwd_fp8(p, causal != 0, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 

@@ -80,3 +80,33 @@ def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, bound: np.ndarray, what: st
     assert (err <= tol).all(), f"{what}: {int((err > tol).sum())} entries over tolerance; {stats}"
     assert err.mean() <= GRAD_MEAN_C * bound.mean(), f"{what}: mean error; {stats}"
     return stats
+
+
+# ------------------------------------------------------------------------------- FP8 path
+# Tolerance of the FP8 forward against exact attention of its dequantized inputs.  The kernel
+# adds the E4M3 rounding of every probability it feeds the P V product (relative error <= 2^-4,
+# half a 3-bit-mantissa spacing) to fp32 accumulation; so |O - O_ref| <= 2^-4 A elementwise with
+# A = sum_k P_k |V_k| / l.  The test allows 2^-3 A on top of the bf16 rounding of O, a mean error
+# of at most 2^-5 mean(A), and the LSE bound of the bf16 path (the scores themselves are exact
+# products of the codes).
+FP8_C = 2.0 ** -3
+FP8_MEAN_C = 2.0 ** -5
+
+
+def check_fp8(o_gpu, lse_gpu, o_ref, lse_ref, a_bound, what=""):
+    assert np.isfinite(o_gpu).all() and np.isfinite(lse_gpu).all(), f"{what}: non-finite"
+    err = np.abs(o_gpu - o_ref)
+    tol = acc.bf16_half_ulp(o_ref) + FP8_C * a_bound
+    stats = {"o_max_abs": float(err.max()), "max_err_over_tol": float((err / tol).max()),
+             "mean_over_bound": float(err.mean() / a_bound.mean()),
+             "lse_max_abs": float(np.abs(lse_gpu - lse_ref).max())}
+    assert (err <= tol).all(), f"{what}: {int((err > tol).sum())} O values over tolerance; {stats}"
+    assert err.mean() <= FP8_MEAN_C * a_bound.mean(), f"{what}: mean error; {stats}"
+    assert np.abs(lse_gpu - lse_ref).max() <= LSE_ABS, f"{what}: LSE; {stats}"
+    return stats
+
+
+def fp8_bound(q, k, v, causal, scale):
+    """A = P |V| (rows of P sum to one) for one head of dequantized float64 inputs."""
+    from oracle import attention as orc
+    return orc.probabilities(q, k, causal, scale) @ np.abs(v)

@@ -182,3 +182,21 @@ def test_bwd_validation(lib):
     assert call_bwd(scale=float("nan")) == -7
     assert call_bwd(ws=None) == -8 and call_bwd(ws=A + 16) == -8 and call_bwd(ws_bytes=100) == -8
     assert call_bwd(N=0) == 0 and call_bwd(H=0, dq=None) == 0
+
+
+def test_fp8_validation(lib):
+    A = ALIGNED
+    q = lib.attn_quantize_fp8
+    assert q(A, A, A, 1, 2, 300, 96, 0, None) == -2
+    assert q(None, A, A, 1, 2, 300, 128, 0, None) == -1
+    assert q(A, A + 8, A, 1, 2, 300, 128, 1, None) == -4
+    assert q(A, A, A + 2, 1, 2, 300, 128, 1, None) == -4
+    assert q(A, A, A, -1, 2, 300, 128, 0, None) == -3
+    assert q(A, A, A, 1, 2, 0, 128, 0, None) == 0
+    f = lib.attn_fwd_fp8
+    assert f(A, A, A, A, A, A, A, A, 1, 2, 300, 64, 0, 0.1, None) == -2    # head dim 128 only
+    assert f(A, A, None, A, A, A, A, A, 1, 2, 300, 128, 0, 0.1, None) == -1
+    assert f(A, A, A, A, A + 8, A, A, A, 1, 2, 300, 128, 0, 0.1, None) == -4
+    assert f(A, A + 2, A, A, A, A, A, A, 1, 2, 300, 128, 0, 0.1, None) == -4
+    assert f(A, A, A, A, A, A, A, A, 1, 2, 300, 128, 0, -1.0, None) == -7
+    assert f(A, A, A, A, A, A, A, A, 1, 0, 300, 128, 0, 0.1, None) == 0
