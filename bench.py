@@ -386,6 +386,56 @@ def run_ours(args, w, rank, world, dist):
                    "speedup": ms_one / ms_auto, "launches_per_step": 2 if chosen > 1 else 1}
         del sq, sk, sv, so, sl, sws
 
+    # ---- FP8 (E4M3) forward on the same shape: quantize once, then time the FP8 kernel; the
+    # quantization of Q, K and V (three launches) is timed separately
+    fp8 = None
+    if not args.no_extras and w.d == 128:
+        q8, sq = attn.quantize_fp8(q)
+        k8, sk = attn.quantize_fp8(k)
+        vt8, sv = attn.quantize_fp8(v, transpose=True)
+        fo8 = torch.empty_like(o)
+        fl8 = torch.empty_like(lse)
+
+        def fp8_step():
+            attn.attn_fwd_fp8(q8, sq, k8, sk, vt8, sv, causal=w.causal, scale=w.scale, out=fo8,
+                              lse=fl8)
+
+        for _ in range(3):
+            fp8_step()
+        barrier()
+        evs = []
+        for _ in range(50):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fp8_step()
+            e1.record(stream)
+            evs.append((e0, e1))
+        barrier()
+        f_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        evs = []
+        for _ in range(10):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.quantize_fp8(q)
+            attn.quantize_fp8(k)
+            attn.quantize_fp8(v, transpose=True)
+            e1.record(stream)
+            evs.append((e0, e1))
+        barrier()
+        qz_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        fp8_peak = float(peaks["bf16_tflops"]) * 2.0
+        fp8 = {"workload": w.name, "ms": f_ms, "tflops": flops / (f_ms * 1e-3) / 1e12,
+               "frac_of_fp8_peak": flops / (f_ms * 1e-3) / 1e12 / fp8_peak,
+               "fp8_peak": fp8_peak,
+               "fp8_peak_source": "measured bf16 burst x 2 (nominal dense fp8/bf16 ratio)",
+               "speedup_vs_bf16": kernel_ms / f_ms, "quantize_qkv_ms": qz_ms,
+               "launches_per_step": 1}
+        del q8, k8, vt8, sq, sk, sv, fo8, fl8
+
     # ---- backward pass on the same shape (non-causal and causal): dQ, dK, dV from the
     # forward's O and LSE and a random upstream gradient
     backward = None
@@ -444,7 +494,7 @@ def run_ours(args, w, rank, world, dist):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "unfused": unfused,
-            "gqa": gqa, "splitkv": splitkv, "backward": backward,
+            "gqa": gqa, "splitkv": splitkv, "backward": backward, "fp8": fp8,
             "clocks": clock_info, "gpu_launches": args.steps,
             "kernel_ms_median": statistics.median(per),
         }
@@ -463,7 +513,7 @@ def main():
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the grouped-query, split-KV and backward measurements")
+                    help="skip the grouped-query, split-KV, FP8 and backward measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
