@@ -123,8 +123,8 @@ ATTN_API int attn_fwd_splitkv_slices(int B, int H, int N, int num_splits);
 
 /*
  * Workspace bytes attn_fwd_splitkv needs: with S the slice count it will use, an fp32 partial
- * output [S][B*H*N][d] followed by three fp32 planes [3][S][B*H*N] (slice max in log2 units, the
- * exact row sum, the row sum of the bf16-rounded weights), each region rounded up to 256 bytes.
+ * output [S][B*H*N][d] followed by two fp32 planes [2][S][B*H*N] (slice max in log2 units, the
+ * row sum), each region rounded up to 256 bytes.
  * Returns 0 when S is 1 (no workspace needed) or the sizes are invalid.
  */
 ATTN_API size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);

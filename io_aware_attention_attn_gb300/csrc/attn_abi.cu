@@ -180,11 +180,11 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
-// Split-KV workspace: partial O [S][B H N][d] fp32, then [3][S][B H N] fp32 statistics.
+// Split-KV workspace: partial O [S][B H N][d] fp32, then [2][S][B H N] fp32 statistics.
 static size_t splitkv_bytes(int B, int H, int N, int d, int S) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t o_bytes = (static_cast<size_t>(S) * rows * d * 4 + 255) / 256 * 256;
-  return o_bytes + (3 * static_cast<size_t>(S) * rows * 4 + 255) / 256 * 256;
+  return o_bytes + (2 * static_cast<size_t>(S) * rows * 4 + 255) / 256 * 256;
 }
 
 }  // namespace attn

@@ -22,11 +22,10 @@
 // complete (a commit barrier) before issuing it: tcgen05 MMAs with different accumulators are not
 // ordered with respect to each other.
 //
-// Softmax in the exp2 domain: t = s * scale * log2(e), p = 2^(t - m).  The reference maximum m
-// moves only when a tile raises the row maximum by more than kTau (log2 units); O and l always
-// share the reference, so O / l is unchanged (the correction factor is applied exactly when the
-// reference moves).  O is divided by the sum of the bf16-rounded P (the weights the tensor cores
-// used); lse uses the sum of the unrounded values.
+// Softmax in the exp2 domain: t = s * scale * log2(e), p = 2^(t - m).  The reference m is a row
+// maximum of some earlier tile; a tile is first exponentiated against it, and the tile's maximum
+// is taken (and m moved to it, O and l rescaled) only on the first tile or when the tile's row sum
+// exceeds kSumLimit.  O and l always share the reference, so O / l is unchanged.  O is divided by, and lse takes, the fp32 sum of the unrounded P.
 #pragma once
 
 #include <cuda.h>
@@ -361,7 +360,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const float sl2 = p.scale_log2;
     float m2 = -INFINITY;            // reference max of the scaled scores (log2 units)
     float le[4] = {0.f, 0.f, 0.f, 0.f};  // sums of 2^(t - m), fp32
-    float lr[4] = {0.f, 0.f, 0.f, 0.f};  // the same values after rounding to bf16
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!(ok = mbar_wait_warp(bar(Lay::bSF + t), static_cast<uint32_t>(j) & 1u, wc, 2, 8)))
@@ -390,46 +388,63 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         #pragma unroll
         for (int c = 0; c < kBN; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
-      float mx[8];
-      #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = s[k];
-      #pragma unroll
-      for (int c = 8; c < kBN; c += 16)
+      // P = 2^(t - m) in bf16, two per 32-bit word, over the first 64 columns of S_t (written in
+      // two halves so each half's words are dead once stored); ts = this tile's row sums.
+      // Pass 0 exponentiates against the current reference; the row maximum is taken (pass 1)
+      // only on the first tile or when a row's tile sum exceeds kSumLimit (every P then stays
+      // <= kSumLimit).  Both passes are warp-uniform: the TMEM stores are collective.
+      float ts[4];
+      bool moved = false;
+      float alpha = 1.f;
+      bool need = (j == 0);
+      #pragma unroll 1
+      for (int pass = (j == 0) ? 1 : 0; pass < 2; ++pass) {
+        float m_use = m2;
+        if (pass == 1) {
+          float mx[8];
+          #pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = s[k];
+          #pragma unroll
+          for (int c = 8; c < kBN; c += 16)
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[c + k], s[c + 8 + k]);
+          const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7])) * sl2;
+          const float m_new = need ? fmaxf(mt, m2) : m2;
+          moved = (m_new != m2);
+          m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha = moved ? ex2_approx(m2 - m_use) : 1.f;
+          m2 = m_new;
+          if (moved) {
+            #pragma unroll
+            for (int k = 0; k < 4; ++k) le[k] *= alpha;
+          }
+          tmem_wait_st();  // pass 0's stores land before these overwrite them
+        }
+        const float neg_m = -m_use;
         #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[c + k], s[c + 8 + k]);
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                             fmaxf(mx[6], mx[7])) * sl2;
-      const float m_new = (mt > m2 + kTau) ? mt : m2;
-      const bool moved = (m_new != m2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = moved ? ex2_approx(m2 - m_use) : 1.f;
-      m2 = m_new;
-      if (moved) {
+        for (int k = 0; k < 4; ++k) ts[k] = 0.f;
         #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          le[k] *= alpha;
-          lr[k] *= alpha;
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+          #pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 64 * h + 2 * i;
+            float x0, x1;
+            ffma2(x0, x1, s[c], s[c + 1], sl2, sl2, neg_m, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            pk[i] = pack_bf16x2(p0, p1);
+            fadd2(ts[2 * (i & 1)], ts[2 * (i & 1) + 1], p0, p1);
+          }
+          tmem_st32(s_col + 32 * h, pk);
+        }
+        if (pass == 0) {
+          need = !(((ts[0] + ts[1]) + (ts[2] + ts[3])) <= kSumLimit);  // also catches inf, NaN
+          if (!__any_sync(0xffffffffu, need)) break;
         }
       }
-
-      // P = 2^(t - m) in bf16, two per 32-bit word, over the first 64 columns of S_t; written in
-      // two halves so each half's words are dead once stored
-      const float neg_m = -m_use;
       #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-        #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = 64 * h + 2 * i;
-          float x0, x1;
-          ffma2(x0, x1, s[c], s[c + 1], sl2, sl2, neg_m, neg_m);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          pk[i] = pack_bf16x2(p0, p1);
-          fadd2(le[2 * (i & 1)], le[2 * (i & 1) + 1], p0, p1);
-          add_bf16x2_f32(lr[2 * (i & 1)], lr[2 * (i & 1) + 1], pk[i]);
-        }
-        tmem_st32(s_col + 32 * h, pk);
-      }
+      for (int k = 0; k < 4; ++k) le[k] += ts[k];
 
       // O_t holds P_t V up to key tile j-1 (that product completed before S_t was rewritten);
       // bring it to the new reference max before P_t V_j is added
@@ -450,7 +465,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     if (n > 0 && ok) ok = mbar_wait_warp(bar(Lay::bOD + t), 0, wc, 2, 9);
     const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
-    const float l_round = (lr[0] + lr[1]) + (lr[2] + lr[3]);
     const bool valid = row < seq_len;
     const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
                         static_cast<size_t>(y0) + static_cast<size_t>(row);
@@ -464,7 +478,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (valid) {
         p.part_stat[slot] = has ? m2 : -INFINITY;
         p.part_stat[plane + slot] = has ? l_exact : 0.f;
-        p.part_stat[2 * plane + slot] = has ? l_round : 0.f;
       }
       if (has) {
         tc_fence_after();
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
     } else if (n > 0 && ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l_round;
+      const float inv_l = 1.f / l_exact;
       uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);
       #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

@@ -12,7 +12,9 @@ namespace attn {
 
 constexpr int kBM = 128;           // query rows per tile
 constexpr int kBN = 128;           // keys per tile
-constexpr float kTau = 8.0f;       // tolerated growth of the row max before O is rescaled (log2)
+// A tile is exponentiated against the running reference maximum first; only when its row sum
+// exceeds kSumLimit (so no P exceeds it either) is the tile maximum taken and the reference moved.
+constexpr float kSumLimit = 65536.f;
 
 struct FwdParams {
   CUtensorMap tm_q;          // 3-D maps {d, rows, heads}, box {64, 128, 1}, 128-byte swizzle

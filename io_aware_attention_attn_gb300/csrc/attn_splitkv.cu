@@ -1,7 +1,7 @@
 // attn_splitkv.cu -- merge of split-KV partial results into O and lse.
 //
 // Each key slice s of a query row left an unnormalised output a_s, a reference maximum m_s (log2
-// units) and its sums l_s (exact and of the bf16-rounded weights).  The merge is the block merge
+// units) and its fp32 row sum l_s.  The merge is the block merge
 // of the CS336 GPU/attention notes, "Online softmax 回顾", applied to all slices at once:
 //   M = max_s m_s,  w_s = 2^(m_s - M),  O = sum_s w_s a_s / sum_s w_s l_s,
 //   lse = (M + log2 sum_s w_s l_s) * ln 2.
@@ -31,14 +31,13 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
   float acc[kPer];
   #pragma unroll
   for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-  float le = 0.f, lr = 0.f;
+  float le = 0.f;
   for (int s = 0; s < S; ++s) {
     const long long slot = s * rows + row;
     const float m = stat[slot];
     if (m == -INFINITY) continue;  // this slice held no key of the row
     const float w = ex2_approx(m - M);
     le += w * stat[plane + slot];
-    lr += w * stat[2 * plane + slot];
     const float* src = part_o + slot * D + lane * kPer;
     if constexpr (kPer == 4) {
       const float4 x = *reinterpret_cast<const float4*>(src);
@@ -48,7 +47,7 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
       acc[0] += w * x.x; acc[1] += w * x.y;
     }
   }
-  const float inv = 1.f / lr;
+  const float inv = 1.f / le;
   __nv_bfloat16* dst = o + row * D + lane * kPer;
   if constexpr (kPer == 4) {
     *reinterpret_cast<uint2*>(dst) =

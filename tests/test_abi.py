@@ -114,16 +114,16 @@ def test_splitkv_workspace_bytes(lib):
     # B=1, H=2, N=8192: 64 query pairs over 64 key tiles; cost(1) = 66, cost(2) = 1 wave x 34,
     # cost(3) = 2 waves x 24 -> 2 slices
     rows = 1 * 2 * 8192
-    assert f(1, 2, 8192, 128, 0) == 2 * rows * 128 * 4 + 3 * 2 * rows * 4
+    assert f(1, 2, 8192, 128, 0) == 2 * rows * 128 * 4 + 2 * 2 * rows * 4
     # B=1, H=1, N=16384: 64 pairs, 128 key tiles; 7 slices (3 waves x 21) beat 2 (1 x 66)
     rows = 16384
-    assert f(1, 1, 16384, 64, 0) == 7 * rows * 64 * 4 + 3 * 7 * rows * 4
-    assert f(1, 2, 8192, 128, 5) == 5 * 2 * 8192 * 128 * 4 + 3 * 5 * 2 * 8192 * 4
+    assert f(1, 1, 16384, 64, 0) == 7 * rows * 64 * 4 + 2 * 7 * rows * 4
+    assert f(1, 2, 8192, 128, 5) == 5 * 2 * 8192 * 128 * 4 + 2 * 5 * 2 * 8192 * 4
     # an explicit count above the 8 key tiles of N=1000 is lowered to 8 (regions 256-aligned)
     rows = 1000
     o_bytes = -(-8 * rows * 64 * 4 // 256) * 256
-    assert f(1, 1, 1000, 64, 100) == o_bytes + -(-3 * 8 * rows * 4 // 256) * 256
-    assert f(1, 1, 1 << 20, 64, 1000) == 32 * (1 << 20) * 64 * 4 + 3 * 32 * (1 << 20) * 4
+    assert f(1, 1, 1000, 64, 100) == o_bytes + -(-2 * 8 * rows * 4 // 256) * 256
+    assert f(1, 1, 1 << 20, 64, 1000) == 32 * (1 << 20) * 64 * 4 + 2 * 32 * (1 << 20) * 4
     assert f(1, 2, 8192, 128, 1) == 0        # one slice: plain fused forward, no workspace
     assert f(2, 32, 4096, 128, 0) == 0       # 1024 pairs already fill the GPU
     assert f(1, 1, 100, 64, 4) == 0          # a single key tile cannot be split
