@@ -288,8 +288,12 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
         for (int k = 0; k < 4; ++k) le[k] *= alpha;
       }
       // P = 2^(s c - m); codes of P * f, four keys per 32-bit TMEM column
-      const float neg_m = -m_use;
+      // the weights P * f = 2^(s c - m + log2 f) come out of the exponential directly; the row
+      // sums take them back to P with one multiplication per tile
+      const float lf = log2f(f);
+      const float neg_m = lf - m_use;
       uint32_t pk[32];
+      float ts[4] = {0.f, 0.f, 0.f, 0.f};
       #pragma unroll
       for (int i = 0; i < 32; ++i) {
         float x0, x1, x2, x3;
@@ -297,12 +301,15 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
         ffma2(x2, x3, s[4 * i + 2], s[4 * i + 3], c, c, neg_m, neg_m);
         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        fadd2(le[2 * (i & 1)], le[2 * (i & 1) + 1], p0, p1);
-        fadd2(le[2 * (i & 1)], le[2 * (i & 1) + 1], p2, p3);
-        pk[i] = static_cast<uint32_t>(pack_e4m3x2(p0 * f, p1 * f)) |
-                (static_cast<uint32_t>(pack_e4m3x2(p2 * f, p3 * f)) << 16);
+        fadd2(ts[2 * (i & 1)], ts[2 * (i & 1) + 1], p0, p1);
+        fadd2(ts[2 * (i & 1)], ts[2 * (i & 1) + 1], p2, p3);
+        pk[i] = static_cast<uint32_t>(pack_e4m3x2(p0, p1)) |
+                (static_cast<uint32_t>(pack_e4m3x2(p2, p3)) << 16);
       }
       tmem_st32(s_col, pk);
+      const float inv_f = ex2_approx(-lf);
+      #pragma unroll
+      for (int k = 0; k < 4; ++k) le[k] = fmaf(ts[k], inv_f, le[k]);
       if (j > 0 && __any_sync(0xffffffffu, moved)) {
         #pragma unroll
         for (int cc = 0; cc < 128 / 32; ++cc) {
