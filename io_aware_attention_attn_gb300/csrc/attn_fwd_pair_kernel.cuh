@@ -425,18 +425,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         #pragma unroll
         for (int k = 0; k < 4; ++k) ts[k] = 0.f;
         #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+        for (int h = 0; h < 4; ++h) {  // quarters of 32 keys: 16 packed words each
+          uint32_t pk[16];
           #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 64 * h + 2 * i;
+          for (int i = 0; i < 16; ++i) {
+            const int c = 32 * h + 2 * i;
             float x0, x1;
             ffma2(x0, x1, s[c], s[c + 1], sl2, sl2, neg_m, neg_m);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             pk[i] = pack_bf16x2(p0, p1);
             fadd2(ts[2 * (i & 1)], ts[2 * (i & 1) + 1], p0, p1);
           }
-          tmem_st32(s_col + 32 * h, pk);
+          tmem_st16(s_col + 16 * h, pk);
         }
         if (pass == 0) {
           need = !(((ts[0] + ts[1]) + (ts[2] + ts[3])) <= kSumLimit);  // also catches inf, NaN
