@@ -235,7 +235,7 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
                   part_stat);
 }
 
-// Backward workspace: two fp32 planes [B*H][n_pad] (lse * log2(e), then D), each rounded up to
+// Backward workspace: two fp32 planes [B*H][n_pad] (-lse * log2(e), then -D), each rounded up to
 // 256 bytes.
 static size_t bwd_plane_bytes(int B, int H, int N) {
   const size_t n_pad = (static_cast<size_t>(N) + kBM - 1) / kBM * kBM;
@@ -272,10 +272,10 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  float* lse2 = static_cast<float*>(workspace);
-  float* dd = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plane);
-  p.lse2 = lse2;
-  p.dd = dd;
+  float* nlse2 = static_cast<float*>(workspace);
+  float* nd = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plane);
+  p.nlse2 = nlse2;
+  p.nd = nd;
   p.status = status_word();
   if (!p.status) return ATTN_ERR_LAUNCH;
   p.B = B;
@@ -286,7 +286,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_bwd_prep(o, dout, lse, lse2, dd, B * H, N, p.n_pad, d, st);
+  cudaError_t e = launch_bwd_prep(o, dout, lse, nlse2, nd, B * H, N, p.n_pad, d, st);
   if (e == cudaSuccess)
     e = (d == 64) ? launch_bwd_d64(p, causal != 0, st) : launch_bwd_d128(p, causal != 0, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;

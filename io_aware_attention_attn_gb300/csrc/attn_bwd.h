@@ -4,7 +4,7 @@
 // Lecture 5 notes, section 6.2, "反向传播怎么办") and applies the chain rule of the definition:
 // dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with D_i = dO_i . O_i, dQ = scale dS K,
 // dK = scale dS^T Q.  Three launches:
-//   bwd_prep_kernel         D_i and lse_i * log2(e) per query row, into padded fp32 planes
+//   bwd_prep_kernel         -D_i and -lse_i * log2(e) per query row, into padded fp32 planes
 //   attn_bwd_dkdv_kernel    one CTA per (head, 128-key tile): dK and dV accumulated in tensor
 //                           memory over the query tiles
 //   attn_bwd_dq_kernel      one CTA per (head, 128-query tile): dQ accumulated in tensor memory
@@ -33,8 +33,8 @@ struct BwdParams {
   __nv_bfloat16* dq;  // outputs [B, H, N, D] bf16
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  const float* lse2;  // [B*H][n_pad]: lse * log2(e); +inf in rows >= N
-  const float* dd;    // [B*H][n_pad]: rowsum(dO * O); 0 in rows >= N
+  const float* nlse2;  // [B*H][n_pad]: -lse * log2(e); -inf in rows >= N
+  const float* nd;     // [B*H][n_pad]: -rowsum(dO * O); 0 in rows >= N
   int* status;        // device status word (bounded waits)
   int B, H, N;
   int n_tiles;        // ceil(N / 128)
@@ -52,7 +52,7 @@ struct BwdKvLayout {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;                    // [kBwdStages]
   static constexpr int kDO = kQ + kBwdStages * kTile;      // [kBwdStages]
-  static constexpr int kVec = kDO + kBwdStages * kTile;    // [kBwdStages] x (lse2[128], D[128])
+  static constexpr int kVec = kDO + kBwdStages * kTile;    // [kBwdStages] x (-lse2[128], -D[128])
   static constexpr int kBar = kVec + kBwdStages * 1024;
   enum {
     bKV = 0,                  // K_j and V_j landed
@@ -106,7 +106,7 @@ static_assert(BwdQLayout<128>::kDynBytes <= 232448, "dQ kernel exceeds 227 KB sh
 // Launchers (one translation unit per head dimension for the tile kernels).
 cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, cudaStream_t stream);
-cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2,
-                            float* dd, int BH, int N, int n_pad, int d, cudaStream_t stream);
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* nlse2,
+                            float* nd, int BH, int N, int n_pad, int d, cudaStream_t stream);
 
 }  // namespace attn

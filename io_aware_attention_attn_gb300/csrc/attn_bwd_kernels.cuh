@@ -162,8 +162,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d_hint(sbase + Lay::kV + c * 16384, &p.tm_v, bar(Lay::bKV), c * 64, j * kBN, z,
                          once);
       }
-      const float* lse2 = p.lse2 + static_cast<size_t>(z) * p.n_pad;
-      const float* dd = p.dd + static_cast<size_t>(z) * p.n_pad;
+      const float* nlse2 = p.nlse2 + static_cast<size_t>(z) * p.n_pad;
+      const float* nd = p.nd + static_cast<size_t>(z) * p.n_pad;
       int issued = 0;
       bool ok = true;
       for (int t = 0; t < n_it; ++t) {
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d_hint(sbase + Lay::kDO + s * Lay::kTile + c * 16384, &p.tm_do,
                            bar(Lay::bQF + s), c * 64, i * kBM, z, keep);
         }
-        bulk_load_1d(sbase + Lay::kVec + s * 1024, lse2 + i * kBM, 512, bar(Lay::bQF + s));
-        bulk_load_1d(sbase + Lay::kVec + s * 1024 + 512, dd + i * kBM, 512, bar(Lay::bQF + s));
+        bulk_load_1d(sbase + Lay::kVec + s * 1024, nlse2 + i * kBM, 512, bar(Lay::bQF + s));
+        bulk_load_1d(sbase + Lay::kVec + s * 1024 + 512, nd + i * kBM, 512, bar(Lay::bQF + s));
         ++issued;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
@@ -280,12 +280,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l = reinterpret_cast<const float4*>(vec)[c4];
-        pf[4 * c4 + 0] = ex2_approx(fmaf(pf[4 * c4 + 0], sl2, -l.x));
-        pf[4 * c4 + 1] = ex2_approx(fmaf(pf[4 * c4 + 1], sl2, -l.y));
-        pf[4 * c4 + 2] = ex2_approx(fmaf(pf[4 * c4 + 2], sl2, -l.z));
-        pf[4 * c4 + 3] = ex2_approx(fmaf(pf[4 * c4 + 3], sl2, -l.w));
+      for (int c4 = 0; c4 < 16; ++c4) {  // P = 2^(s scale log2e - lse2): packed FMAs, then ex2
+        const float4 l = reinterpret_cast<const float4*>(vec)[c4];  // -lse2 of 4 queries
+        float x0, x1, x2, x3;
+        ffma2(x0, x1, pf[4 * c4], pf[4 * c4 + 1], sl2, sl2, l.x, l.y);
+        ffma2(x2, x3, pf[4 * c4 + 2], pf[4 * c4 + 3], sl2, sl2, l.z, l.w);
+        pf[4 * c4 + 0] = ex2_approx(x0);
+        pf[4 * c4 + 1] = ex2_approx(x1);
+        pf[4 * c4 + 2] = ex2_approx(x2);
+        pf[4 * c4 + 3] = ex2_approx(x3);
       }
       if (CAUSAL && i == j) {  // diagonal tile: query 64*half + c precedes key r when < r
         #pragma unroll
@@ -309,24 +312,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld32(col_dp + 32, u1);
         tmem_wait_ld_regs(u0);
         tmem_wait_ld_regs(u1);
-        const float* dvec = vec + 128;
+        const float* dvec = vec + 128;  // -D of this half's 64 queries
         uint32_t pk[32];
         #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
+        for (int c4 = 0; c4 < 16; ++c4) {  // dS = P (dP - D): packed add and multiply
           const float4 dl = reinterpret_cast<const float4*>(dvec)[c4];
-          const int c = 4 * c4;
-          pk[2 * c4] = pack_bf16x2(pf[c] * (bwd::u2f(u0[c]) - dl.x), pf[c + 1] * (bwd::u2f(u0[c + 1]) - dl.y));
-          pk[2 * c4 + 1] =
-              pack_bf16x2(pf[c + 2] * (bwd::u2f(u0[c + 2]) - dl.z), pf[c + 3] * (bwd::u2f(u0[c + 3]) - dl.w));
-        }
-        #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 dl = reinterpret_cast<const float4*>(dvec)[8 + c4];
-          const int c = 4 * c4;
-          pk[16 + 2 * c4] = pack_bf16x2(pf[32 + c] * (bwd::u2f(u1[c]) - dl.x),
-                                        pf[32 + c + 1] * (bwd::u2f(u1[c + 1]) - dl.y));
-          pk[16 + 2 * c4 + 1] = pack_bf16x2(pf[32 + c + 2] * (bwd::u2f(u1[c + 2]) - dl.z),
-                                            pf[32 + c + 3] * (bwd::u2f(u1[c + 3]) - dl.w));
+          const uint32_t* u = c4 < 8 ? u0 : u1;
+          const int c = 4 * (c4 & 7);
+          float t0, t1, t2, t3, d0, d1, d2, d3;
+          fadd2_to(t0, t1, bwd::u2f(u[c]), bwd::u2f(u[c + 1]), dl.x, dl.y);
+          fadd2_to(t2, t3, bwd::u2f(u[c + 2]), bwd::u2f(u[c + 3]), dl.z, dl.w);
+          fmul2(d0, d1, pf[4 * c4], pf[4 * c4 + 1], t0, t1);
+          fmul2(d2, d3, pf[4 * c4 + 2], pf[4 * c4 + 3], t2, t3);
+          pk[2 * c4] = pack_bf16x2(d0, d1);
+          pk[2 * c4 + 1] = pack_bf16x2(d2, d3);
         }
         tmem_st32(col_dp, pk);
       }
@@ -517,8 +516,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t col_s = t_lane + kColS + 64 * half;
     const uint32_t col_dp = t_lane + kColDP + 64 * half;
     const float sl2 = p.scale_log2;
-    const float lse2 = p.lse2[static_cast<size_t>(z) * p.n_pad + row];
-    const float dd = p.dd[static_cast<size_t>(z) * p.n_pad + row];
+    const float nlse2 = p.nlse2[static_cast<size_t>(z) * p.n_pad + row];  // -lse * log2(e)
+    const float nd = p.nd[static_cast<size_t>(z) * p.n_pad + row];        // -D
     bool ok = true;
     for (int jj = 0; jj < n_kv; ++jj) {
       const uint32_t par = static_cast<uint32_t>(jj) & 1u;
@@ -540,7 +539,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(Lay::bSR));  // S columns may be rewritten
       #pragma unroll
-      for (int c = 0; c < 64; ++c) pf[c] = ex2_approx(fmaf(pf[c], sl2, -lse2));
+      for (int c = 0; c < 64; c += 2) {
+        float x0, x1;
+        ffma2(x0, x1, pf[c], pf[c + 1], sl2, sl2, nlse2, nlse2);
+        pf[c] = ex2_approx(x0);
+        pf[c + 1] = ex2_approx(x1);
+      }
       // keys past the end of the sequence, and (diagonal tile) keys after the query, get P = 0
       const int key0 = jj * kBN + 64 * half;
       if ((CAUSAL && jj == i) || key0 + 64 > p.N) {
@@ -558,13 +562,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_ld_regs(u1);
         uint32_t pk[32];
         #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[c] = pack_bf16x2(pf[2 * c] * (bwd::u2f(u0[2 * c]) - dd),
-                              pf[2 * c + 1] * (bwd::u2f(u0[2 * c + 1]) - dd));
-        #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[16 + c] = pack_bf16x2(pf[32 + 2 * c] * (bwd::u2f(u1[2 * c]) - dd),
-                                   pf[32 + 2 * c + 1] * (bwd::u2f(u1[2 * c + 1]) - dd));
+        for (int c = 0; c < 32; ++c) {  // dS = P (dP - D): packed add and multiply
+          const uint32_t* u = c < 16 ? u0 : u1;
+          const int k = 2 * (c & 15);
+          float t0, t1, d0, d1;
+          fadd2_to(t0, t1, bwd::u2f(u[k]), bwd::u2f(u[k + 1]), nd, nd);
+          fmul2(d0, d1, pf[2 * c], pf[2 * c + 1], t0, t1);
+          pk[c] = pack_bf16x2(d0, d1);
+        }
         tmem_st32(col_dp, pk);
       }
       tmem_wait_st();

@@ -1,8 +1,9 @@
 // attn_bwd_prep.cu -- per-row inputs of the backward tile kernels.
 //
 // D_i = dO_i . O_i (the softmax-gradient term: sum_k P_ik dP_ik = dO_i . O_i because
-// sum_k P_ik V_k = O_i) and lse_i * log2(e), written to [B*H][n_pad] fp32 planes whose rows
-// past N hold D = 0 and lse2 = +inf, so that a padded query row rebuilds P = 2^(-inf) = 0.
+// sum_k P_ik V_k = O_i) and lse_i * log2(e), written negated to [B*H][n_pad] fp32 planes (the
+// tile kernels add them with packed adds and fused multiply-adds); rows past N hold -D = 0 and
+// -lse2 = -inf, so that a padded query row rebuilds P = 2^(-inf) = 0.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -16,8 +17,8 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout,
                                                        const float* __restrict__ lse,
-                                                       float* __restrict__ lse2,
-                                                       float* __restrict__ dd, long long rows_pad,
+                                                       float* __restrict__ nlse2,
+                                                       float* __restrict__ nd, long long rows_pad,
                                                        int N, int n_pad) {
   constexpr int kPer = D / 32;  // elements per lane
   const long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -27,8 +28,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   const int row = static_cast<int>(w % n_pad);
   if (row >= N) {
     if (lane == 0) {
-      lse2[w] = INFINITY;
-      dd[w] = 0.f;
+      nlse2[w] = -INFINITY;
+      nd[w] = 0.f;
     }
     return;
   }
@@ -53,25 +54,25 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
-    dd[w] = acc;
-    lse2[w] = lse[static_cast<size_t>(z) * N + row] * 1.4426950408889634f;
+    nd[w] = -acc;
+    nlse2[w] = -lse[static_cast<size_t>(z) * N + row] * 1.4426950408889634f;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2,
-                            float* dd, int BH, int N, int n_pad, int d, cudaStream_t stream) {
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* nlse2,
+                            float* nd, int BH, int N, int n_pad, int d, cudaStream_t stream) {
   const long long rows_pad = static_cast<long long>(BH) * n_pad;
   const long long blocks = (rows_pad + 7) / 8;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const auto* ob = static_cast<const __nv_bfloat16*>(o);
   const auto* db = static_cast<const __nv_bfloat16*>(dout);
   if (d == 64)
-    bwd_prep_kernel<64><<<static_cast<int>(blocks), 256, 0, stream>>>(ob, db, lse, lse2, dd,
+    bwd_prep_kernel<64><<<static_cast<int>(blocks), 256, 0, stream>>>(ob, db, lse, nlse2, nd,
                                                                       rows_pad, N, n_pad);
   else
-    bwd_prep_kernel<128><<<static_cast<int>(blocks), 256, 0, stream>>>(ob, db, lse, lse2, dd,
+    bwd_prep_kernel<128><<<static_cast<int>(blocks), 256, 0, stream>>>(ob, db, lse, nlse2, nd,
                                                                        rows_pad, N, n_pad);
   return cudaGetLastError();
 }
