@@ -72,27 +72,29 @@ struct BwdKvLayout {
   static constexpr int kDynBytes = kBytes + 1024;
 };
 
-// dQ kernel: Q_i and dO_i resident; K_j and V_j stream through kBwdStages rings.
+// dQ kernel: Q_i and dO_i resident; K_j and V_j stream through rings (K three deep: K_j is
+// still read by dQ_j while S_{j+1} reads K_{j+1} and K_{j+2} is in flight).
+constexpr int kBwdStagesQK = 3;
 template <int D>
 struct BwdQLayout {
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTile;
-  static constexpr int kK = kDO + kTile;                   // [kBwdStages]
-  static constexpr int kV = kK + kBwdStages * kTile;       // [kBwdStages]
+  static constexpr int kK = kDO + kTile;                   // [kBwdStagesQK]
+  static constexpr int kV = kK + kBwdStagesQK * kTile;     // [kBwdStages]
   static constexpr int kBar = kV + kBwdStages * kTile;
   enum {
     bQ = 0,                   // Q_i and dO_i landed
-    bKF = 1,                  // K stage full [kBwdStages]
-    bKE = bKF + kBwdStages,   // K stage free [kBwdStages]
-    bVF = bKE + kBwdStages,   // V stage full [kBwdStages]
+    bKF = 1,                  // K stage full [kBwdStagesQK]
+    bKE = bKF + kBwdStagesQK, // K stage free [kBwdStagesQK]
+    bVF = bKE + kBwdStagesQK, // V stage full [kBwdStages]
     bVE = bVF + kBwdStages,   // V stage free [kBwdStages]
     bS = bVE + kBwdStages,    // S = Q K^T written
     bSR,                      // S read by every compute thread (256 arrivals)
-    bDP,                      // dP = dO V^T written
-    bDS,                      // dS (bf16) written over dP (256 arrivals)
-    bDQ,                      // dQ += dS K completed (and every earlier MMA)
-    bDR,                      // drain after an abort
+    bDP,                      // dP = dO V^T written            [2 tensor-memory buffers]
+    bDS = bDP + 2,            // dS (bf16) written over dP       [2] (256 arrivals)
+    bDQ = bDS + 2,            // dQ += dS K from buffer completed [2]
+    bDR = bDQ + 2,            // drain after an abort
     kNumBars
   };
   static constexpr int kMisc = kBar + kNumBars * 8;

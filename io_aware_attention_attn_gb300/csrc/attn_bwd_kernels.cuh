@@ -371,17 +371,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Lay::bQ), 1);
-    for (int s = 0; s < kBwdStages; ++s) {
+    for (int s = 0; s < kBwdStagesQK; ++s) {
       mbar_init(bar(Lay::bKF + s), 1);
       mbar_init(bar(Lay::bKE + s), 1);
+    }
+    for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(bar(Lay::bVF + s), 1);
       mbar_init(bar(Lay::bVE + s), 1);
     }
     mbar_init(bar(Lay::bS), 1);
     mbar_init(bar(Lay::bSR), 8 * 32);
-    mbar_init(bar(Lay::bDP), 1);
-    mbar_init(bar(Lay::bDS), 8 * 32);
-    mbar_init(bar(Lay::bDQ), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(Lay::bDP + b), 1);
+      mbar_init(bar(Lay::bDS + b), 8 * 32);
+      mbar_init(bar(Lay::bDQ + b), 1);
+    }
     mbar_init(bar(Lay::bDR), 1);
     fence_barrier_init();
     misc[1] = 0;
@@ -409,7 +413,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  // S at 0, dQ at 256, dP / dS double-buffered at 128 and 384 (key tile jj uses buffer jj & 1)
+  constexpr uint32_t kColS = 0, kColDQ = 256;
+  constexpr uint32_t kColDP[2] = {128, 384};
   constexpr uint64_t kTileD = static_cast<uint64_t>(Lay::kTile >> 4);
 
   if (warp == 0) {
@@ -432,28 +438,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int nk = 0, nv = 0;
       bool ok = true;
       for (int jj = 0; jj < n_kv; ++jj) {
-        const int s = jj % kBwdStages;
-        const uint32_t free_par = (static_cast<uint32_t>(jj / kBwdStages) & 1u) ^ 1u;
-        if (jj >= kBwdStages && !(ok = mbar_wait(bar(Lay::bKE + s), free_par, wc, 0, 1))) break;
-        mbar_arrive_expect_tx(bar(Lay::bKF + s), Lay::kTile);
+        const int sk = jj % kBwdStagesQK, sv = jj % kBwdStages;
+        if (jj >= kBwdStagesQK &&
+            !(ok = mbar_wait(bar(Lay::bKE + sk),
+                             (static_cast<uint32_t>(jj / kBwdStagesQK) & 1u) ^ 1u, wc, 0, 1)))
+          break;
+        mbar_arrive_expect_tx(bar(Lay::bKF + sk), Lay::kTile);
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d_hint(sbase + Lay::kK + s * Lay::kTile + c * 16384, &p.tm_k,
-                           bar(Lay::bKF + s), c * 64, jj * kBN, z, keep);
+          tma_load_3d_hint(sbase + Lay::kK + sk * Lay::kTile + c * 16384, &p.tm_k,
+                           bar(Lay::bKF + sk), c * 64, jj * kBN, z, keep);
         ++nk;
-        if (jj >= kBwdStages && !(ok = mbar_wait(bar(Lay::bVE + s), free_par, wc, 0, 2))) break;
-        mbar_arrive_expect_tx(bar(Lay::bVF + s), Lay::kTile);
+        if (jj >= kBwdStages &&
+            !(ok = mbar_wait(bar(Lay::bVE + sv),
+                             (static_cast<uint32_t>(jj / kBwdStages) & 1u) ^ 1u, wc, 0, 2)))
+          break;
+        mbar_arrive_expect_tx(bar(Lay::bVF + sv), Lay::kTile);
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d_hint(sbase + Lay::kV + s * Lay::kTile + c * 16384, &p.tm_v,
-                           bar(Lay::bVF + s), c * 64, jj * kBN, z, keep);
+          tma_load_3d_hint(sbase + Lay::kV + sv * Lay::kTile + c * 16384, &p.tm_v,
+                           bar(Lay::bVF + sv), c * 64, jj * kBN, z, keep);
         ++nv;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
         mbar_wait_drain(bar(Lay::bQ), 0);
-        for (int t = (nk > kBwdStages ? nk - kBwdStages : 0); t < nk; ++t)
-          mbar_wait_drain(bar(Lay::bKF + t % kBwdStages),
-                          static_cast<uint32_t>(t / kBwdStages) & 1u);
+        for (int t = (nk > kBwdStagesQK ? nk - kBwdStagesQK : 0); t < nk; ++t)
+          mbar_wait_drain(bar(Lay::bKF + t % kBwdStagesQK),
+                          static_cast<uint32_t>(t / kBwdStagesQK) & 1u);
         for (int t = (nv > kBwdStages ? nv - kBwdStages : 0); t < nv; ++t)
           mbar_wait_drain(bar(Lay::bVF + t % kBwdStages),
                           static_cast<uint32_t>(t / kBwdStages) & 1u);
@@ -468,35 +479,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);          // K-major use
     const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16, 1024);
     const uint64_t desc_k_mn = sdesc_sw128(sbase + Lay::kK, 16384, 1024);    // MN-major use
-    bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 2);
-    for (int jj = 0; ok && jj < n_kv; ++jj) {
-      const int s = jj % kBwdStages;
-      const uint32_t par = static_cast<uint32_t>(jj) & 1u;
-      const uint32_t full_par = static_cast<uint32_t>(jj / kBwdStages) & 1u;
-      if (!(ok = mbar_wait_warp(bar(Lay::bKF + s), full_par, wc, 1, 3))) break;
-      // S_jj rewrites columns the compute threads read S_{jj-1} from
-      if (jj > 0 && !(ok = mbar_wait_warp(bar(Lay::bSR), par ^ 1u, wc, 1, 4))) break;
+    // S and dP of key tile jj + 1 are issued before dQ of tile jj waits for its dS, so the tensor
+    // pipe has them to execute while the compute warps form dS: dP alternates between two
+    // tensor-memory buffers, and a buffer is rewritten once the dQ product that read it (two
+    // tiles back) completed.
+    auto issue_s = [&](int jj) {
+      const int s = jj % kBwdStagesQK;
+      if (!mbar_wait_warp(bar(Lay::bKF + s), static_cast<uint32_t>(jj / kBwdStagesQK) & 1u, wc,
+                          1, 3))
+        return false;
+      // S rewrites the columns the compute threads read S_{jj-1} from
+      if (jj > 0 &&
+          !mbar_wait_warp(bar(Lay::bSR), (static_cast<uint32_t>(jj) & 1u) ^ 1u, wc, 1, 4))
+        return false;
       tc_fence_after();
       if (lane == 0) {
         bwd::mma_ss_tile<D>(tmem + kColS, desc_q, desc_k + s * kTileD, kIdSS);
         mma_commit(bar(Lay::bS));
       }
       __syncwarp();
-      if (!(ok = mbar_wait_warp(bar(Lay::bVF + s), full_par, wc, 1, 5))) break;
-      // dP_jj rewrites the columns dS_{jj-1} was read from: wait for dQ_{jj-1}
-      if (jj > 0 && !(ok = mbar_wait_warp(bar(Lay::bDQ), par ^ 1u, wc, 1, 6))) break;
+      return true;
+    };
+    auto issue_dp = [&](int jj) {
+      const int s = jj % kBwdStages, b = jj & 1;
+      if (!mbar_wait_warp(bar(Lay::bVF + s), static_cast<uint32_t>(jj / kBwdStages) & 1u, wc, 1,
+                          5))
+        return false;
+      if (jj >= 2 &&  // the buffer's previous dS was read by dQ of tile jj - 2
+          !mbar_wait_warp(bar(Lay::bDQ + b), (static_cast<uint32_t>(jj >> 1) & 1u) ^ 1u, wc, 1, 6))
+        return false;
       tc_fence_after();
       if (lane == 0) {
-        bwd::mma_ss_tile<D>(tmem + kColDP, desc_do, desc_v + s * kTileD, kIdSS);
-        mma_commit(bar(Lay::bDP));
+        bwd::mma_ss_tile<D>(tmem + kColDP[b], desc_do, desc_v + s * kTileD, kIdSS);
+        mma_commit(bar(Lay::bDP + b));
         mma_commit(bar(Lay::bVE + s));
       }
       __syncwarp();
-      if (!(ok = mbar_wait_warp(bar(Lay::bDS), par, wc, 1, 7))) break;
+      return true;
+    };
+    bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 2) && issue_s(0) && issue_dp(0);
+    for (int jj = 0; ok && jj < n_kv; ++jj) {
+      const int s = jj % kBwdStagesQK, b = jj & 1;
+      if (jj + 1 < n_kv && !(ok = issue_s(jj + 1) && issue_dp(jj + 1))) break;
+      if (!(ok = mbar_wait_warp(bar(Lay::bDS + b), static_cast<uint32_t>(jj >> 1) & 1u, wc, 1,
+                                7)))
+        break;
       tc_fence_after();
       if (lane == 0) {
-        bwd::mma_ts_tile(tmem + kColDQ, tmem + kColDP, desc_k_mn + s * kTileD, kIdTS, jj > 0);
-        mma_commit(bar(Lay::bDQ));
+        bwd::mma_ts_tile(tmem + kColDQ, tmem + kColDP[b], desc_k_mn + s * kTileD, kIdTS, jj > 0);
+        mma_commit(bar(Lay::bDQ + b));
         mma_commit(bar(Lay::bKE + s));
       }
       __syncwarp();
@@ -514,7 +545,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = i * kBM + r;        // query row within the sequence (padded rows < n_pad)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t col_s = t_lane + kColS + 64 * half;
-    const uint32_t col_dp = t_lane + kColDP + 64 * half;
     const float sl2 = p.scale_log2;
     const float nlse2 = p.nlse2[static_cast<size_t>(z) * p.n_pad + row];  // -lse * log2(e)
     const float nd = p.nd[static_cast<size_t>(z) * p.n_pad + row];        // -D
@@ -552,7 +582,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         #pragma unroll
         for (int c = 0; c < 64; ++c) pf[c] = (c < lim) ? pf[c] : 0.f;
       }
-      if (!(ok = mbar_wait_warp(bar(Lay::bDP), par, wc, 2, 9))) break;
+      const int b = jj & 1;
+      const uint32_t col_dp = t_lane + kColDP[b] + 64 * half;
+      if (!(ok = mbar_wait_warp(bar(Lay::bDP + b), static_cast<uint32_t>(jj >> 1) & 1u, wc, 2, 9)))
+        break;
       tc_fence_after();
       {
         uint32_t u0[32], u1[32];
@@ -574,9 +607,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(Lay::bDS));
+      mbar_arrive(bar(Lay::bDS + b));
     }
-    if (ok) ok = mbar_wait_warp(bar(Lay::bDQ), static_cast<uint32_t>(n_kv - 1) & 1u, wc, 2, 10);
+    // the last dQ commit covers every MMA of the CTA
+    if (ok)
+      ok = mbar_wait_warp(bar(Lay::bDQ + ((n_kv - 1) & 1)),
+                          static_cast<uint32_t>((n_kv - 1) >> 1) & 1u, wc, 2, 10);
     if (ok) {
       tc_fence_after();
       const bool valid = row < p.N;
