@@ -6,7 +6,8 @@ in HBM.  ``value`` is whole-job TFLOPS (4*B*H*N^2*d per step, summed over ranks,
 rank time).  Timing: W untimed warm-up steps, then K steps timed with CUDA events on the
 launching stream, an L2 flush (a 256 MiB write) before each step outside the events, barrier and
 synchronize on both sides.  Extra keys: ``e2e`` (the same metric through the public API with
-pinned host buffers and the host<->device copies inside the timed region), ``roofline`` (the
+pinned host buffers and every step's host<->device copies inside the timed region, steps
+pipelined over two device buffers; the serial loop beside it), ``roofline`` (the
 kernel against the measured bf16 tensor peak), ``cpu_baseline`` (the float64 oracle on a bounded
 sample), ``unfused`` (the three-kernel comparison path) and ``clocks``.
 
@@ -252,39 +253,89 @@ def run_ours(args, w, rank, world, dist):
                 "peak_source": f"{peaks['_source']} bf16 burst (cuBLAS)",
                 "algorithmic_bytes": acc.attention_ideal_bytes(w.H, w.B * w.N, w.d)}
 
-    # ---- end to end through the public API: pinned host -> device, forward, device -> host
+    # ---- end to end through the public API: pinned host -> device, forward, device -> host.
+    # Every step copies its own Q, K, V in and its O and LSE out; steps are pipelined over two
+    # device buffers (inputs of step i+1 copied in on one stream and outputs of step i-1 copied
+    # out on another while step i computes), as a data loader would.  The plain serial loop is
+    # reported beside it.
     e2e = None
     if not args.no_e2e:
-        hq = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-        hk = torch.from_numpy(k_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-        hv = torch.from_numpy(v_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-        ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
-        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
         n_e2e = max(3, min(args.steps, 50))
+        h_in = [[torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+                 for x in (q_np, k_np, v_np)] for _ in range(2)]
+        h_out = [(torch.empty(o.shape, dtype=torch.bfloat16).pin_memory(),
+                  torch.empty(lse.shape, dtype=torch.float32).pin_memory()) for _ in range(2)]
+        d_in = [[torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)] for _ in range(2)]
+        d_out = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
+        s_h2d = torch.cuda.Stream(dev)
+        s_d2h = torch.cuda.Stream(dev)
 
-        def e2e_step():
-            dq = hq.to(dev, non_blocking=True)
-            dk = hk.to(dev, non_blocking=True)
-            dv = hv.to(dev, non_blocking=True)
-            oo, ll = attn.attn_fwd(dq, dk, dv, causal=w.causal, scale=w.scale)
-            ho.copy_(oo, non_blocking=True)
-            hl.copy_(ll, non_blocking=True)
+        def run_pipelined(n):
+            ev_in = [torch.cuda.Event() for _ in range(2)]
+            ev_done = [torch.cuda.Event() for _ in range(2)]
+            ev_out = [torch.cuda.Event() for _ in range(2)]
+            used = [False, False]
 
-        for _ in range(3):
-            e2e_step()
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        barrier()
-        e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+            def h2d(i):
+                b = i % 2
+                with torch.cuda.stream(s_h2d):
+                    if used[b]:
+                        s_h2d.wait_event(ev_done[b])  # the buffer's previous step has computed
+                    for dst, src in zip(d_in[b], h_in[b]):
+                        dst.copy_(src, non_blocking=True)
+                    ev_in[b].record(s_h2d)
+
+            h2d(0)
+            for i in range(n):
+                b = i % 2
+                if i + 1 < n:
+                    h2d(i + 1)
+                stream.wait_event(ev_in[b])
+                if used[b]:
+                    stream.wait_event(ev_out[b])  # the buffer's previous outputs left the device
+                attn.attn_fwd(d_in[b][0], d_in[b][1], d_in[b][2], causal=w.causal,
+                              scale=w.scale, out=d_out[b][0], lse=d_out[b][1], stream=stream)
+                ev_done[b].record(stream)
+                used[b] = True
+                with torch.cuda.stream(s_d2h):
+                    s_d2h.wait_event(ev_done[b])
+                    h_out[b][0].copy_(d_out[b][0], non_blocking=True)
+                    h_out[b][1].copy_(d_out[b][1], non_blocking=True)
+                    ev_out[b].record(s_d2h)
+            stream.wait_stream(s_h2d)
+            stream.wait_stream(s_d2h)
+
+        def run_serial(n):
+            for _ in range(n):
+                dq_ = h_in[0][0].to(dev, non_blocking=True)
+                dk_ = h_in[0][1].to(dev, non_blocking=True)
+                dv_ = h_in[0][2].to(dev, non_blocking=True)
+                oo, ll = attn.attn_fwd(dq_, dk_, dv_, causal=w.causal, scale=w.scale)
+                h_out[0][0].copy_(oo, non_blocking=True)
+                h_out[0][1].copy_(ll, non_blocking=True)
+
+        def timed(fn):
+            fn(3)
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(n_e2e)
+            e1.record(stream)
+            barrier()
+            return max_over_ranks(e0.elapsed_time(e1), dist, dev)
+
+        e_ms = timed(run_pipelined)
+        s_ms = timed(run_serial)
+        if not np.array_equal(h_out[(n_e2e - 1) % 2][0].view(torch.int16).numpy(),
+                              o.view(torch.int16).cpu().numpy()):
+            raise RuntimeError("end-to-end output differs from the device-resident run")
         e2e = {"value": flops * n_e2e * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "h2d_bytes_per_step": 3 * q.numel() * 2,
-               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4, "steps": n_e2e}
-        del hq, hk, hv, ho, hl
+               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4, "steps": n_e2e,
+               "pipelined": "two device buffers; H2D of step i+1 and D2H of step i-1 overlap step i",
+               "serial_value": flops * n_e2e * world / (s_ms * 1e-3) / 1e12}
+        del h_in, h_out, d_in, d_out
 
     # ---- unfused three-kernel comparison path (memory wall)
     unfused = None
