@@ -73,7 +73,9 @@ typedef enum {
  * tensor cores, then writes O = acc / l in bf16 and lse = m + ln l in fp32.  The N x N score
  * matrix never reaches HBM; causal tiles above the diagonal are skipped.
  *   q, k, v : bf16 inputs (read only)          o   : bf16 output, same layout as q
- *   lse     : fp32 output                      cu_seqlens : NULL (dense) or int32[B+1] (packed)
+ *   lse     : fp32 output                      cu_seqlens : NULL (dense) or int32[B+1] (packed;
+ *                                                           a prefix sum from 0 to N, else the
+ *                                                           status word reports kind 2)
  *   B, H, N, d, causal, scale : as described above; stream : cudaStream_t
  * Returns an attn_status.
  */
@@ -233,9 +235,12 @@ ATTN_API int attn_fwd_unfused_noalloc(const void* q, const void* k, const void* 
 /*
  * Device-side status of the kernels launched on `stream` since the previous call: 0 if every
  * pipeline wait completed; otherwise a code whose low byte is 1 (a wait exceeded its time limit,
- * after which the kernel drained its in-flight copies, released its tensor memory and returned),
- * bits 8..15 name the waiting role and bits 16..23 the wait site.  Synchronises `stream`, then
- * clears the status.  Returns ATTN_ERR_LAUNCH (< 0) if the status cannot be read.
+ * after which the kernel drained its in-flight copies, released its tensor memory and returned;
+ * bits 8..15 name the waiting role and bits 16..23 the wait site) or 2 (the cu_seqlens given to a
+ * packed-batch call was not a non-decreasing prefix sum from 0 to N; the kernel computed on its
+ * offsets clamped into [0, N] and read or wrote nothing outside the tensors).  The first problem
+ * recorded is kept.  Synchronises `stream`, then clears the status.  Returns ATTN_ERR_LAUNCH (< 0)
+ * if the status cannot be read.
  */
 ATTN_API int attn_get_last_device_error(void* stream);
 

@@ -102,6 +102,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // cu_seqlens are clamped to [0, N] so no access leaves the buffers
       int remaining = blockIdx.x / p.H;
       int f_start = 0, f_len = 0, f_pt = -1;
+      if (blockIdx.x == 0) {
+        // one CTA checks that cu_seqlens is a prefix sum from 0 to N (non-decreasing); a bad one
+        // is reported through the status word, and every CTA works on offsets clamped into [0, N]
+        bool bad = false;
+        for (int s = lane; s < p.B; s += 32) {
+          const int a = __ldg(p.cu_seqlens + s), b = __ldg(p.cu_seqlens + s + 1);
+          bad |= (b < a) || (s == 0 && a != 0) || (s == p.B - 1 && b != p.N);
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(p.status, 0, kStatusBadSeqlens);
+      }
       for (int base = 0; base < p.B; base += 32) {
         const int s = base + lane;
         int start = 0, len = 0;

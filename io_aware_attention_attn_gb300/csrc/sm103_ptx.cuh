@@ -14,7 +14,9 @@ namespace attn {
 // status word (kind | role << 8 | site << 16), sets the CTA's abort flag and returns false; the
 // kernel then unwinds (drains its copies and MMAs, frees tensor memory) instead of hanging.
 // --------------------------------------------------------------------------------------------
-enum : int { kStatusTimeout = 1 };
+// kinds (low byte of the status word): a bounded wait ran out; cu_seqlens was not a valid prefix
+// sum of lengths (the kernel then computed on offsets clamped into [0, N])
+enum : int { kStatusTimeout = 1, kStatusBadSeqlens = 2 };
 // A wait gives up after this many nanoseconds of %globaltimer (one second).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 

@@ -33,3 +33,25 @@ def test_wait_timeout_reports_and_context_survives():
     o_ref, lse_ref = orc.attention_dense(q, k, v, True, w.scale)
     check(to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "after timeout")
     assert attn.last_device_error() == 0
+
+
+@pytest.mark.gpu
+def test_bad_cu_seqlens_is_reported_not_faulted():
+    # a decreasing offset: the kernel clamps every offset into [0, N], computes, and reports kind 2
+    import math
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from io_aware_attention_attn_gb300 import build
+    build.build()
+    q, k, v, _ = configs.custom_varlen(950, [100, 200], 2, 64, True)
+    bad = torch.tensor([0, 150, 100, 300], dtype=torch.int32, device="cuda")
+    assert attn.last_device_error() == 0
+    attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), cu_seqlens=bad, causal=True,
+                  scale=1 / math.sqrt(64))
+    code = attn.last_device_error()
+    assert attn.decode_status(code)["kind"] == 2, code
+    assert attn.last_device_error() == 0  # cleared by the read
+    good = torch.tensor([0, 100, 300], dtype=torch.int32, device="cuda")
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), cu_seqlens=good, causal=True,
+                           scale=1 / math.sqrt(64))
+    assert attn.last_device_error() == 0 and torch.isfinite(lse).all()
