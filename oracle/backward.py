@@ -103,3 +103,32 @@ def blocked_backward_head(q, k, v, o, lse, do, causal: bool, scale: float, block
             dq[i0:i1] += scale * (ds @ k[j0:j1])
             dk[j0:j1] += scale * (ds.T @ q[i0:i1])
     return dq, dk, dv
+
+
+def attention_gqa_bwd_dense(q, k, v, do, causal: bool, scale: float):
+    """Gradients of grouped-query attention (CS336 Lecture 5 notes, section 6.3: query head h
+    reads K/V head h // (H // H_kv)), dense: q, do [B, H, N, d]; k, v [B, H_kv, N, d].
+
+    A K/V head feeds every query head of its group, so its gradients are the sums of the
+    per-query-head gradients over the group (the chain rule through a shared input).
+    Returns (dq [B,H,N,d], dk [B,H_kv,N,d], dv [B,H_kv,N,d], o [B,H,N,d], lse [B,H,N]).
+    """
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    group = H // H_kv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            g = h // group
+            r = attention_bwd_head(q[b, h], k[b, g], v[b, g], do[b, h], causal, scale)
+            dq[b, h] = r[0]
+            dk[b, g] += r[1]
+            dv[b, g] += r[2]
+            o[b, h] = r[3]
+            lse[b, h] = r[4]
+    return dq, dk, dv, o, lse

@@ -182,3 +182,40 @@ def _mut_unmasked_dv(q, k, v, do, c, s):  # P rebuilt without the causal mask fo
                                     _mut_dq_transposed, _mut_d_from_dp, _mut_unmasked_dv])
 def test_pins_catch_planted_mistake(mutant):
     assert pin_failures(mutant), f"{mutant.__name__} slipped through every pin"
+
+
+# ----------------------------------------------------------------- grouped-query backward
+def _gqa_loss(q, k, v, do, causal, scale):
+    o, _ = orc.attention_gqa_dense(q, k, v, causal, scale)
+    return float(np.sum(do * o))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_backward_finite_differences(causal):
+    rng = np.random.default_rng(77)
+    B, H, H_kv, N, d = 1, 4, 2, 5, 3
+    q = rng.uniform(-1, 1, (B, H, N, d))
+    k = rng.uniform(-1, 1, (B, H_kv, N, d))
+    v = rng.uniform(-1, 1, (B, H_kv, N, d))
+    do = rng.uniform(-1, 1, (B, H, N, d))
+    dq, dk, dv, _, _ = bwd.attention_gqa_bwd_dense(q, k, v, do, causal, 0.6)
+    eps = 1e-6
+    for t, x, g in ((0, q, dq), (1, k, dk), (2, v, dv)):
+        for idx in np.ndindex(x.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[t][idx] += eps
+            lp = _gqa_loss(*args, do, causal, 0.6)
+            args[t][idx] -= 2 * eps
+            lm = _gqa_loss(*args, do, causal, 0.6)
+            assert abs((lp - lm) / (2 * eps) - g[idx]) <= 1e-7 * (1 + abs(g[idx]))
+
+
+def test_gqa_backward_with_all_heads_is_multi_head():
+    q = inputs.bf16_normal(81, (2, 3, 40, 8))
+    k = inputs.bf16_normal(82, (2, 3, 40, 8))
+    v = inputs.bf16_normal(83, (2, 3, 40, 8))
+    do = inputs.bf16_normal(84, (2, 3, 40, 8))
+    a = bwd.attention_gqa_bwd_dense(q, k, v, do, True, 0.3)
+    b = bwd.attention_bwd_dense(q, k, v, do, True, 0.3)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, atol=1e-13)
