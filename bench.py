@@ -525,7 +525,30 @@ def run_ours(args, w, rank, world, dist):
                 "launches_per_step": 3}
             del fo, fl
         backward["workload"] = w.name
-        del dout, bws, gq, gk, gv
+        # grouped-query backward on the GQA shape (dK, dV summed over each group of 4)
+        gw = configs.GQA
+        gq_np, gk_np, gv_np, _ = gw.make()
+        gqd, gkd, gvd = to_dev(gq_np), to_dev(gk_np), to_dev(gv_np)
+        gdo = to_dev(gw.make_dout())
+        fo, fl = attn.attn_fwd(gqd, gkd, gvd, causal=False, scale=gw.scale)
+        for _ in range(3):
+            attn.attn_bwd(gqd, gkd, gvd, fo, fl, gdo, scale=gw.scale, workspace=bws)
+        barrier()
+        evs = []
+        for _ in range(30):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.attn_bwd(gqd, gkd, gvd, fo, fl, gdo, scale=gw.scale, workspace=bws)
+            e1.record(stream)
+            evs.append((e0, e1))
+        barrier()
+        g_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        g_flops = acc.attention_bwd_flops(gw.H, [gw.N] * gw.B, gw.d, False)
+        backward["gqa_non_causal"] = {"workload": gw.name, "ms": g_ms,
+                                      "tflops": g_flops / (g_ms * 1e-3) / 1e12}
+        del dout, bws, gq, gk, gv, gqd, gkd, gvd, gdo, fo, fl
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

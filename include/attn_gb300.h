@@ -155,6 +155,19 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
                       size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass of grouped-query / multi-query attention (CS336 Lecture 5 notes, section 6.3):
+ * as attn_bwd, except that k, v, dk and dv have H_kv heads ([B, H_kv, N, d]) and query head h
+ * reads K/V head h / (H / H_kv).  A K/V head's gradients are the sums over the query heads that
+ * share it: the dK/dV kernel runs one CTA per (K/V head, key tile) that visits the query tiles of
+ * all of them, so the sums accumulate in tensor memory and each element is still written once.
+ * H_kv must divide H, else ATTN_ERR_SHAPE.  The workspace is attn_bwd_workspace_bytes(B,H,N,d).
+ */
+ATTN_API int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          int B, int H, int H_kv, int N, int d, int causal, float scale,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Workspace bytes attn_bwd needs: two fp32 planes of B * H * Npad values (Npad = N rounded up to
  * 128), each rounded up to 256 bytes.  Returns 0 for invalid sizes.
  */

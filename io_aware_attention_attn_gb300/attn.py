@@ -31,6 +31,8 @@ SIGNATURES = {
     "attn_fwd_splitkv_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
     "attn_fwd_splitkv_slices": (_I, [_I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "attn_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
+                          _S, _P]),
     "attn_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -184,9 +186,10 @@ def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
              workspace=None, dq=None, dk=None, dv=None, stream=None):
     """Backward pass: gradients (dQ, dK, dV) of the fused forward for the upstream gradient
-    ``dout``, given the forward's ``o`` and ``lse``.  Dense [B, H, N, d] only."""
+    ``dout``, given the forward's ``o`` and ``lse``.  Dense [B, H, N, d]; k and v may have fewer
+    heads than q (grouped-query: attn_bwd_gqa, dK and dV summed over each group)."""
     import torch
-    B, H, _, N, d = _check_inputs(q, k, v, None)
+    B, H, H_kv, N, d = _check_inputs(q, k, v, None, allow_kv_heads=True)
     for name, t in (("o", o), ("dout", dout)):
         if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != q.shape or \
                 t.device != q.device:
@@ -202,13 +205,19 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
     with torch.cuda.device(q.device):
-        rc = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                            dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
-                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                            _stream_handle(stream, q.device))
-    _check("attn_bwd", rc)
+        st = _stream_handle(stream, q.device)
+        if H_kv == H:
+            rc = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale), *ws, st)
+        else:
+            rc = lib().attn_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), B, H, H_kv, N, d, int(bool(causal)),
+                                    float(scale), *ws, st)
+    _check("attn_bwd_gqa" if H_kv != H else "attn_bwd", rc)
     return dq, dk, dv
 
 

@@ -247,13 +247,15 @@ extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
   return 2 * bwd_plane_bytes(B, H, N);
 }
 
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                        int H, int N, int d, int causal, float scale, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+static int bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                    int H, int Hkv, int N, int d, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, void* stream) {
   bool empty = false;
   int rc = validate(q, k, v, o, lse, nullptr, B, H, N, d, scale, &empty);
-  if (rc != ATTN_OK || empty) return rc;
+  if (rc != ATTN_OK) return rc;
+  if (Hkv < 0 || (H > 0 && (Hkv == 0 || H % Hkv != 0))) return ATTN_ERR_SHAPE;
+  if (empty) return ATTN_OK;
   if (!dout || !dq || !dk || !dv) return ATTN_ERR_NULL;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return ATTN_ERR_ALIGN;
@@ -264,11 +266,14 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if ((rc = check_device()) != 0) return rc;
   BwdParams p{};
   const uint64_t heads = static_cast<uint64_t>(B) * H;
+  const uint64_t kv_heads = static_cast<uint64_t>(B) * Hkv;
   if (encode_rows_map(&p.tm_q, q, d, N, heads) != CUDA_SUCCESS ||
-      encode_rows_map(&p.tm_k, k, d, N, heads) != CUDA_SUCCESS ||
-      encode_rows_map(&p.tm_v, v, d, N, heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_k, k, d, N, kv_heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_v, v, d, N, kv_heads) != CUDA_SUCCESS ||
       encode_rows_map(&p.tm_do, dout, d, N, heads) != CUDA_SUCCESS)
     return ATTN_ERR_LAUNCH;
+  p.H_kv = Hkv;
+  p.group = H / Hkv;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
@@ -290,6 +295,22 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (e == cudaSuccess)
     e = (d == 64) ? launch_bwd_d64(p, causal != 0, st) : launch_bwd_d128(p, causal != 0, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int H, int N, int d, int causal, float scale, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, H, N, d, causal, scale, workspace,
+                  workspace_bytes, stream);
+}
+
+extern "C" int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            int B, int H, int H_kv, int N, int d, int causal, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, H_kv, N, d, causal, scale, workspace,
+                  workspace_bytes, stream);
 }
 
 extern "C" int attn_quantize_fp8(const void* x, void* codes, float* scales, int B, int H, int N,

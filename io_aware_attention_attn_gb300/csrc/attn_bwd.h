@@ -37,6 +37,8 @@ struct BwdParams {
   const float* nd;     // [B*H][n_pad]: -rowsum(dO * O); 0 in rows >= N
   int* status;        // device status word (bounded waits)
   int B, H, N;
+  int H_kv;           // key/value heads (H_kv divides H; query head h reads K/V head h / group)
+  int group;          // H / H_kv
   int n_tiles;        // ceil(N / 128)
   int n_pad;          // n_tiles * 128
   float scale_log2;   // scale * log2(e)

@@ -31,10 +31,9 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = allow_smem(kv, kKvSmem, kv_done);
   if (e == cudaSuccess) e = allow_smem(qk, kQSmem, q_done);
   if (e != cudaSuccess) return e;
-  const int grid = p.n_tiles * p.B * p.H;
-  kv<<<grid, kBwdThreads, kKvSmem, stream>>>(p);
+  kv<<<p.n_tiles * p.B * p.H_kv, kBwdThreads, kKvSmem, stream>>>(p);  // per K/V head
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  qk<<<grid, kBwdThreads, kQSmem, stream>>>(p);
+  qk<<<p.n_tiles * p.B * p.H, kBwdThreads, kQSmem, stream>>>(p);      // per query head
   return cudaGetLastError();
 }
 

@@ -119,19 +119,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     misc[1] = 0;
   }
 
-  // key tile j of head slice z; causal: query tiles j .. n_tiles-1 (the most first), else all
-  const int BH = p.B * p.H;
+  // key tile j of K/V head slice z (of B * H_kv); it visits, for each of the `group` query heads
+  // that share the K/V head, query tiles j .. n_tiles-1 (causal; the most first) or all of them.
+  // dK and dV sum over all of them (grouped-query attention: a shared K/V head's gradient is the
+  // sum over its query heads).
+  const int BHkv = p.B * p.H_kv;
   const int L = static_cast<int>(blockIdx.x);
   int z, j;
   if constexpr (CAUSAL) {
-    j = L / BH;
-    z = L % BH;
+    j = L / BHkv;
+    z = L % BHkv;
   } else {  // the key tiles of a head together: its Q and dO tiles stay in L2
     z = L / p.n_tiles;
     j = L % p.n_tiles;
   }
   const int i0 = CAUSAL ? j : 0;
-  const int n_it = p.n_tiles - i0;
+  const int n_head = p.n_tiles - i0;     // query tiles per query head
+  const int n_it = n_head * p.group;     // over the group's query heads
+  const int zq0 = (z / p.H_kv) * p.H + (z % p.H_kv) * p.group;  // first query head slice
 
   __syncthreads();
   if (warp == 1) {
@@ -162,8 +167,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d_hint(sbase + Lay::kV + c * 16384, &p.tm_v, bar(Lay::bKV), c * 64, j * kBN, z,
                          once);
       }
-      const float* nlse2 = p.nlse2 + static_cast<size_t>(z) * p.n_pad;
-      const float* nd = p.nd + static_cast<size_t>(z) * p.n_pad;
       int issued = 0;
       bool ok = true;
       for (int t = 0; t < n_it; ++t) {
@@ -172,17 +175,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             !(ok = mbar_wait(bar(Lay::bQE + s),
                              (static_cast<uint32_t>(t / kBwdStages) & 1u) ^ 1u, wc, 0, 1)))
           break;
-        const int i = i0 + t;
+        const int i = i0 + t % n_head;
+        const int zq = zq0 + t / n_head;
+        const size_t vrow = static_cast<size_t>(zq) * p.n_pad + static_cast<size_t>(i) * kBM;
         mbar_arrive_expect_tx(bar(Lay::bQF + s), 2 * Lay::kTile + 1024);
         #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           tma_load_3d_hint(sbase + Lay::kQ + s * Lay::kTile + c * 16384, &p.tm_q,
-                           bar(Lay::bQF + s), c * 64, i * kBM, z, keep);
+                           bar(Lay::bQF + s), c * 64, i * kBM, zq, keep);
           tma_load_3d_hint(sbase + Lay::kDO + s * Lay::kTile + c * 16384, &p.tm_do,
-                           bar(Lay::bQF + s), c * 64, i * kBM, z, keep);
+                           bar(Lay::bQF + s), c * 64, i * kBM, zq, keep);
         }
-        bulk_load_1d(sbase + Lay::kVec + s * 1024, nlse2 + i * kBM, 512, bar(Lay::bQF + s));
-        bulk_load_1d(sbase + Lay::kVec + s * 1024 + 512, nd + i * kBM, 512, bar(Lay::bQF + s));
+        bulk_load_1d(sbase + Lay::kVec + s * 1024, p.nlse2 + vrow, 512, bar(Lay::bQF + s));
+        bulk_load_1d(sbase + Lay::kVec + s * 1024 + 512, p.nd + vrow, 512, bar(Lay::bQF + s));
         ++issued;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int t = 0; t < n_it; ++t) {
       const int s = t % kBwdStages;
       const uint32_t par = static_cast<uint32_t>(t) & 1u;
-      const int i = i0 + t;
+      const int i = i0 + t % n_head;
       if (!(ok = mbar_wait_warp(bar(Lay::bQF + s), static_cast<uint32_t>(t / kBwdStages) & 1u,
                                 wc, 2, 8)))
         break;
@@ -403,6 +408,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     i = L % p.n_tiles;
   }
   const int n_kv = CAUSAL ? i + 1 : p.n_tiles;
+  const int z_kv = (z / p.H) * p.H_kv + (z % p.H) / p.group;  // K/V head slice of query head z
 
   __syncthreads();
   if (warp == 1) {
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kK + sk * Lay::kTile + c * 16384, &p.tm_k,
-                           bar(Lay::bKF + sk), c * 64, jj * kBN, z, keep);
+                           bar(Lay::bKF + sk), c * 64, jj * kBN, z_kv, keep);
         ++nk;
         if (jj >= kBwdStages &&
             !(ok = mbar_wait(bar(Lay::bVE + sv),
@@ -457,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kV + sv * Lay::kTile + c * 16384, &p.tm_v,
-                           bar(Lay::bVF + sv), c * 64, jj * kBN, z, keep);
+                           bar(Lay::bVF + sv), c * 64, jj * kBN, z_kv, keep);
         ++nv;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits

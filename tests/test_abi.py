@@ -200,3 +200,15 @@ def test_fp8_validation(lib):
     assert f(A, A + 2, A, A, A, A, A, A, 1, 2, 300, 128, 0, 0.1, None) == -4
     assert f(A, A, A, A, A, A, A, A, 1, 2, 300, 128, 0, -1.0, None) == -7
     assert f(A, A, A, A, A, A, A, A, 1, 0, 300, 128, 0, 0.1, None) == 0
+
+
+def test_bwd_gqa_validation(lib):
+    f = lib.attn_bwd_gqa
+    A = ALIGNED
+
+    def c(H, H_kv, d=128, N=300):
+        return f(A, A, A, A, A, A, A, A, A, 1, H, H_kv, N, d, 1, 0.1, A, 1 << 30, None)
+
+    assert c(8, 3) == -3 and c(8, 0) == -3 and c(8, -2) == -3
+    assert c(8, 2, d=96) == -2
+    assert c(0, 0) == 0 and c(8, 2, N=0) == 0

@@ -119,3 +119,37 @@ def test_bwd_full_size_sampled_heads(causal):
     heads = [(0, 0), (1, 17), (1, 31)]
     ref = bwd.attention_bwd_dense(q, k, v, do, causal, w.scale, heads=heads)
     check_all(q, k, v, do, grads, ref, causal, w.scale, w.name, heads=heads)
+
+
+@pytest.mark.parametrize("seed,B,H,H_kv,N,d,causal", [
+    (720, 1, 4, 2, 300, 128, True), (721, 2, 4, 1, 256, 64, False),
+    (722, 1, 6, 3, 129, 128, False), (723, 1, 8, 2, 520, 64, True),
+])
+def test_bwd_gqa(seed, B, H, H_kv, N, d, causal):
+    w = configs.custom(seed, B, H, N, d, causal, H_kv=H_kv)
+    q, k, v, _ = w.make()
+    do = w.make_dout()
+    dq, dk, dv, o_ref, lse_ref = bwd.attention_gqa_bwd_dense(q, k, v, do, causal, w.scale)
+    o = f64_to_bf16_dev(o_ref)
+    lse = torch.from_numpy(lse_ref.astype(np.float32)).cuda()
+    g = attn.attn_bwd(to_dev(q), to_dev(k), to_dev(v), o, lse, to_dev(do), causal=causal,
+                      scale=w.scale)
+    torch.cuda.synchronize()
+    gq, gk, gv = (to_f64(x) for x in g)
+    group = H // H_kv
+    for b in range(B):
+        for h in range(H):
+            qf, kf, vf, dof = (orc.bf16_bits_to_f64(x) for x in
+                               (q[b, h], k[b, h // group], v[b, h // group], do[b, h]))
+            aq, _, _ = grad_bounds(qf, kf, vf, dof, causal, w.scale)
+            check_grad(gq[b, h], dq[b, h], aq, f"{w.name} dQ ({b},{h})")
+        for hk in range(H_kv):
+            # the bound of a summed gradient is the sum of its terms' bounds
+            ak = np.zeros_like(dk[b, hk]); av = np.zeros_like(dv[b, hk])
+            for h in range(hk * group, (hk + 1) * group):
+                qf, kf, vf, dof = (orc.bf16_bits_to_f64(x) for x in
+                                   (q[b, h], k[b, hk], v[b, hk], do[b, h]))
+                _, a_k, a_v = grad_bounds(qf, kf, vf, dof, causal, w.scale)
+                ak += a_k; av += a_v
+            check_grad(gk[b, hk], dk[b, hk], ak, f"{w.name} dK ({b},{hk})")
+            check_grad(gv[b, hk], dv[b, hk], av, f"{w.name} dV ({b},{hk})")
