@@ -168,6 +168,27 @@ ATTN_API int attn_bwd_gqa(const void* q, const void* k, const void* v, const voi
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass on a packed batch of variable-length sequences (the layout of attn_fwd with
+ * cu_seqlens): q, o, dout, dq [H, T, d]; k, v, dk, dv [H_kv, T, d]; lse [H, T]; cu_seqlens
+ * int32[B + 1] on the device, B = number of sequences, T = total rows.  Sequences are independent;
+ * grouped-query heads as attn_bwd_gqa (H_kv = H for multi-head).  The kernels run one CTA per
+ * (head, 128-row tile of a sequence), found by a scan of cu_seqlens; offsets are clamped into
+ * [0, T].  workspace: attn_bwd_varlen_workspace_bytes(B, H, T, d) bytes, 256-byte aligned.
+ * cu_seqlens NULL: ATTN_ERR_NULL.  Returns an attn_status.
+ */
+ATTN_API int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                             const int32_t* cu_seqlens, int B, int H, int H_kv, int T, int d,
+                             int causal, float scale, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
+ * Workspace bytes attn_bwd_varlen needs: two fp32 planes of H * 128 * (ceil(T/128) + B) rows,
+ * each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ */
+ATTN_API size_t attn_bwd_varlen_workspace_bytes(int B, int H, int T, int d);
+
+/*
  * Workspace bytes attn_bwd needs: two fp32 planes of B * H * Npad values (Npad = N rounded up to
  * 128), each rounded up to 256 bytes.  Returns 0 for invalid sizes.
  */

@@ -33,6 +33,9 @@ SIGNATURES = {
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                           _S, _P]),
+    "attn_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                             _F, _P, _S, _P]),
+    "attn_bwd_varlen_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_bwd_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "attn_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -183,13 +186,14 @@ def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(lib().attn_bwd_workspace_bytes(B, H, N, d))
 
 
-def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
-             workspace=None, dq=None, dk=None, dv=None, stream=None):
+def attn_bwd(q, k, v, o, lse, dout, cu_seqlens=None, causal: bool = False,
+             scale: float | None = None, workspace=None, dq=None, dk=None, dv=None, stream=None):
     """Backward pass: gradients (dQ, dK, dV) of the fused forward for the upstream gradient
-    ``dout``, given the forward's ``o`` and ``lse``.  Dense [B, H, N, d]; k and v may have fewer
-    heads than q (grouped-query: attn_bwd_gqa, dK and dV summed over each group)."""
+    ``dout``, given the forward's ``o`` and ``lse``.  Dense [B, H, N, d], or packed [H, T, d] with
+    ``cu_seqlens`` (attn_bwd_varlen); k and v may have fewer heads than q (grouped-query: dK and dV
+    summed over each group)."""
     import torch
-    B, H, H_kv, N, d = _check_inputs(q, k, v, None, allow_kv_heads=True)
+    B, H, H_kv, N, d = _check_inputs(q, k, v, cu_seqlens, allow_kv_heads=True)
     for name, t in (("o", o), ("dout", dout)):
         if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != q.shape or \
                 t.device != q.device:
@@ -199,7 +203,8 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
         raise ValueError("lse must be a contiguous fp32 tensor of shape [B, H, N]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = bwd_workspace_bytes(B, H, N, d)
+    need = (bwd_workspace_bytes(B, H, N, d) if cu_seqlens is None
+            else int(lib().attn_bwd_varlen_workspace_bytes(B, H, N, d)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
@@ -208,7 +213,12 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
     with torch.cuda.device(q.device):
         st = _stream_handle(stream, q.device)
-        if H_kv == H:
+        if cu_seqlens is not None:
+            rc = lib().attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                                       dk.data_ptr(), dv.data_ptr(), cu_seqlens.data_ptr(), B, H,
+                                       H_kv, N, d, int(bool(causal)), float(scale), *ws, st)
+        elif H_kv == H:
             rc = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                 lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                 dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale), *ws, st)
@@ -217,7 +227,8 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
                                     lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                     dv.data_ptr(), B, H, H_kv, N, d, int(bool(causal)),
                                     float(scale), *ws, st)
-    _check("attn_bwd_gqa" if H_kv != H else "attn_bwd", rc)
+    _check("attn_bwd_varlen" if cu_seqlens is not None else
+           ("attn_bwd_gqa" if H_kv != H else "attn_bwd"), rc)
     return dq, dk, dv
 
 

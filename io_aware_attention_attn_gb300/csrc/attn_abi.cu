@@ -297,6 +297,73 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o,
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+// Packed backward workspace: two fp32 planes of H * 128 * (ceil(T/128) + B) rows (one 128-row
+// tile per tile slot of the batch), each rounded up to 256 bytes.
+static size_t bwd_varlen_plane_bytes(int B, int H, int T) {
+  const size_t slots = (static_cast<size_t>(T) + kBM - 1) / kBM + static_cast<size_t>(B);
+  return (static_cast<size_t>(H) * slots * kBM * 4 + 255) / 256 * 256;
+}
+
+extern "C" size_t attn_bwd_varlen_workspace_bytes(int B, int H, int T, int d) {
+  if (B <= 0 || H <= 0 || T < 0 || (d != 64 && d != 128)) return 0;
+  return 2 * bwd_varlen_plane_bytes(B, H, T);
+}
+
+extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               const int32_t* cu_seqlens, int B, int H, int H_kv, int T, int d,
+                               int causal, float scale, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (!cu_seqlens) return ATTN_ERR_NULL;
+  bool empty = false;
+  int rc = validate(q, k, v, o, lse, cu_seqlens, B, H, T, d, scale, &empty);
+  if (rc != ATTN_OK) return rc;
+  if (H_kv < 0 || (H > 0 && (H_kv == 0 || H % H_kv != 0))) return ATTN_ERR_SHAPE;
+  if (empty) return ATTN_OK;
+  if (!dout || !dq || !dk || !dv) return ATTN_ERR_NULL;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_ALIGN;
+  const long long slots = (static_cast<long long>(T) + kBM - 1) / kBM + B;
+  if (slots * H > INT_MAX) return ATTN_ERR_SHAPE;
+  const size_t plane = bwd_varlen_plane_bytes(B, H, T);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      workspace_bytes < 2 * plane)
+    return ATTN_ERR_WORKSPACE;
+  if ((rc = check_device()) != 0) return rc;
+  BwdParams p{};
+  if (encode_rows_map(&p.tm_q, q, d, T, H) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_k, k, d, T, H_kv) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_v, v, d, T, H_kv) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_do, dout, d, T, H) != CUDA_SUCCESS)
+    return ATTN_ERR_LAUNCH;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  float* nlse2 = static_cast<float*>(workspace);
+  float* nd = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plane);
+  p.nlse2 = nlse2;
+  p.nd = nd;
+  p.status = status_word();
+  if (!p.status) return ATTN_ERR_LAUNCH;
+  p.cu_seqlens = cu_seqlens;
+  p.n_seqs = B;
+  p.B = 1;
+  p.H = H;
+  p.N = T;
+  p.H_kv = H_kv;
+  p.group = H / H_kv;
+  p.n_tiles = static_cast<int>(slots);
+  p.n_pad = p.n_tiles * kBM;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      launch_bwd_prep_varlen(o, dout, lse, nlse2, nd, cu_seqlens, B, H, T, p.n_tiles, d, st);
+  if (e == cudaSuccess)
+    e = (d == 64) ? launch_bwd_d64(p, causal != 0, st) : launch_bwd_d128(p, causal != 0, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                         int H, int N, int d, int causal, float scale, void* workspace,

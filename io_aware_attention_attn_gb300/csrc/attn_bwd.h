@@ -36,11 +36,13 @@ struct BwdParams {
   const float* nlse2;  // [B*H][n_pad]: -lse * log2(e); -inf in rows >= N
   const float* nd;     // [B*H][n_pad]: -rowsum(dO * O); 0 in rows >= N
   int* status;        // device status word (bounded waits)
-  int B, H, N;
+  const int32_t* cu_seqlens;  // packed batches: int32[n_seqs + 1] offsets into the T rows; else NULL
+  int n_seqs;         // packed batches: number of sequences
+  int B, H, N;        // packed batches: N = T, the total number of rows
   int H_kv;           // key/value heads (H_kv divides H; query head h reads K/V head h / group)
   int group;          // H / H_kv
-  int n_tiles;        // ceil(N / 128)
-  int n_pad;          // n_tiles * 128
+  int n_tiles;        // dense: ceil(N / 128); packed: tile slots ceil(T / 128) + n_seqs
+  int n_pad;          // rows of a head in the -lse2 / -D planes: 128 * n_tiles
   float scale_log2;   // scale * log2(e)
   float scale;
 };
@@ -69,8 +71,8 @@ struct BwdKvLayout {
     bDR,                      // drain after an abort
     kNumBars
   };
-  static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort flag
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..5] tile
+  static constexpr int kBytes = kMisc + 32;
   static constexpr int kDynBytes = kBytes + 1024;
 };
 
@@ -99,18 +101,65 @@ struct BwdQLayout {
     bDR = bDQ + 2,            // drain after an abort
     kNumBars
   };
-  static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..5] tile
+  static constexpr int kBytes = kMisc + 32;
   static constexpr int kDynBytes = kBytes + 1024;
 };
 
 static_assert(BwdKvLayout<128>::kDynBytes <= 232448, "dK/dV kernel exceeds 227 KB shared memory");
 static_assert(BwdQLayout<128>::kDynBytes <= 232448, "dQ kernel exceeds 227 KB shared memory");
 
+// Packed batches: the 128-row tiles of all sequences, numbered sequence after sequence, are the
+// "slots" of a head.  A warp-collective scan of cu_seqlens maps a slot to its sequence (start
+// row, length, tile within the sequence, slots of the earlier sequences); tile = -1 for a slot past
+// the last tile.  Offsets are clamped into [0, N] so no access leaves the buffers.
+__device__ __forceinline__ void bwd_locate_tile(const int32_t* cu, int n_seqs, int N, int slot,
+                                                int lane, int& start, int& len, int& tile,
+                                                int& base) {
+  start = 0;
+  len = 0;
+  tile = -1;
+  base = 0;
+  int remaining = slot, before = 0;
+  for (int b0 = 0; b0 < n_seqs; b0 += 32) {
+    const int s = b0 + lane;
+    int a = 0, e = 0;
+    if (s < n_seqs) {
+      a = min(max(__ldg(cu + s), 0), N);
+      e = min(max(__ldg(cu + s + 1), a), N);
+    }
+    const int nt = (e - a + kBM - 1) / kBM;
+    int incl = nt;
+    #pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int excl = incl - nt;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (remaining < total) {
+      const unsigned hit = __ballot_sync(0xffffffffu, remaining >= excl && remaining < incl);
+      const int src = __ffs(hit) - 1;  // hit != 0: the slots of this chunk cover `remaining`
+      start = __shfl_sync(0xffffffffu, a, src);
+      len = __shfl_sync(0xffffffffu, e - a, src);
+      const int ex = __shfl_sync(0xffffffffu, excl, src);
+      tile = remaining - ex;
+      base = before + ex;
+      return;
+    }
+    remaining -= total;
+    before += total;
+  }
+}
+
 // Launchers (one translation unit per head dimension for the tile kernels).
 cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_d128(const BwdParams& p, bool causal, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* nlse2,
                             float* nd, int BH, int N, int n_pad, int d, cudaStream_t stream);
+// packed batches: planes of 128 * (ceil(T/128) + n_seqs) rows per head, one 128-row tile per slot
+cudaError_t launch_bwd_prep_varlen(const void* o, const void* dout, const float* lse,
+                                   float* nlse2, float* nd, const int32_t* cu_seqlens, int n_seqs,
+                                   int H, int T, int n_slots, int d, cudaStream_t stream);
 
 }  // namespace attn

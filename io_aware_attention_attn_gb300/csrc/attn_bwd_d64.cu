@@ -21,26 +21,31 @@ cudaError_t allow_smem(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
   return cudaSuccess;
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   static std::atomic<uint64_t> kv_done{0}, q_done{0};
-  auto* kv = attn_bwd_dkdv_kernel<64, CAUSAL>;
-  auto* qk = attn_bwd_dq_kernel<64, CAUSAL>;
+  auto* kv = attn_bwd_dkdv_kernel<64, CAUSAL, VARLEN>;
+  auto* qk = attn_bwd_dq_kernel<64, CAUSAL, VARLEN>;
   constexpr int kKvSmem = BwdKvLayout<64>::kDynBytes;
   constexpr int kQSmem = BwdQLayout<64>::kDynBytes;
   cudaError_t e = allow_smem(kv, kKvSmem, kv_done);
   if (e == cudaSuccess) e = allow_smem(qk, kQSmem, q_done);
   if (e != cudaSuccess) return e;
-  kv<<<p.n_tiles * p.B * p.H_kv, kBwdThreads, kKvSmem, stream>>>(p);  // per K/V head
+  // one CTA per (head, 128-row tile); packed batches: per (head, tile slot), past-the-end slots
+  // return at once
+  const int units = VARLEN ? p.n_tiles : p.n_tiles * p.B;
+  kv<<<units * p.H_kv, kBwdThreads, kKvSmem, stream>>>(p);  // per K/V head
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  qk<<<p.n_tiles * p.B * p.H, kBwdThreads, kQSmem, stream>>>(p);      // per query head
+  qk<<<units * p.H, kBwdThreads, kQSmem, stream>>>(p);      // per query head
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_d64(const BwdParams& p, bool causal, cudaStream_t stream) {
-  return causal ? launch<true>(p, stream) : launch<false>(p, stream);
+  if (p.cu_seqlens)
+    return causal ? launch<true, true>(p, stream) : launch<false, true>(p, stream);
+  return causal ? launch<true, false>(p, stream) : launch<false, false>(p, stream);
 }
 
 }  // namespace attn

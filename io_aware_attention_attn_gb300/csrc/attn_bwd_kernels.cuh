@@ -88,7 +88,7 @@ __device__ __forceinline__ void store_row_half(uint32_t col, float mul, __nv_bfl
 }  // namespace bwd
 
 // =============================================================================== dK / dV kernel
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using Lay = BwdKvLayout<D>;
@@ -123,22 +123,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // that share the K/V head, query tiles j .. n_tiles-1 (causal; the most first) or all of them.
   // dK and dV sum over all of them (grouped-query attention: a shared K/V head's gradient is the
   // sum over its query heads).
-  const int BHkv = p.B * p.H_kv;
+  // Packed batches: z is the K/V head, the tile slot blockIdx.x / H_kv names (sequence, j); rows
+  // are y0 + .. within the packed tensors and the planes' rows of the sequence start at 128 tbase.
   const int L = static_cast<int>(blockIdx.x);
-  int z, j;
-  if constexpr (CAUSAL) {
-    j = L / BHkv;
-    z = L % BHkv;
-  } else {  // the key tiles of a head together: its Q and dO tiles stay in L2
-    z = L / p.n_tiles;
-    j = L % p.n_tiles;
+  int z, j, y0 = 0, seq_len = p.N, tbase = 0;
+  if constexpr (!VARLEN) {
+    const int BHkv = p.B * p.H_kv;
+    if constexpr (CAUSAL) {
+      j = L / BHkv;
+      z = L % BHkv;
+    } else {  // the key tiles of a head together: its Q and dO tiles stay in L2
+      z = L / p.n_tiles;
+      j = L % p.n_tiles;
+    }
+  } else {
+    z = L % p.H_kv;
+    if (warp == 0) {
+      int start, len, tile, base;
+      bwd_locate_tile(p.cu_seqlens, p.n_seqs, p.N, L / p.H_kv, lane, start, len, tile, base);
+      if (lane == 0) {
+        misc[2] = static_cast<uint32_t>(start);
+        misc[3] = static_cast<uint32_t>(len);
+        misc[4] = static_cast<uint32_t>(tile);
+        misc[5] = static_cast<uint32_t>(base);
+      }
+    }
   }
-  const int i0 = CAUSAL ? j : 0;
-  const int n_head = p.n_tiles - i0;     // query tiles per query head
-  const int n_it = n_head * p.group;     // over the group's query heads
-  const int zq0 = (z / p.H_kv) * p.H + (z % p.H_kv) * p.group;  // first query head slice
-
   __syncthreads();
+  if constexpr (VARLEN) {
+    y0 = static_cast<int>(misc[2]);
+    seq_len = static_cast<int>(misc[3]);
+    j = static_cast<int>(misc[4]);
+    tbase = static_cast<int>(misc[5]);
+    if (j < 0) return;  // slot past the last tile of the batch (uniform for the CTA)
+  }
+  const int n_seq_tiles = (seq_len + kBM - 1) / kBM;
+  const int i0 = CAUSAL ? j : 0;
+  const int n_head = n_seq_tiles - i0;   // query tiles per query head
+  const int n_it = n_head * p.group;     // over the group's query heads
+  // first query head slice of the group
+  const int zq0 = VARLEN ? z * p.group : (z / p.H_kv) * p.H + (z % p.H_kv) * p.group;
+
   if (warp == 1) {
     tmem_alloc(sbase + Lay::kMisc, 512);
     tmem_relinquish();
@@ -162,10 +187,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(bar(Lay::bKV), 2 * Lay::kTile);
       #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d_hint(sbase + Lay::kK + c * 16384, &p.tm_k, bar(Lay::bKV), c * 64, j * kBN, z,
-                         once);
-        tma_load_3d_hint(sbase + Lay::kV + c * 16384, &p.tm_v, bar(Lay::bKV), c * 64, j * kBN, z,
-                         once);
+        tma_load_3d_hint(sbase + Lay::kK + c * 16384, &p.tm_k, bar(Lay::bKV), c * 64,
+                         y0 + j * kBN, z, once);
+        tma_load_3d_hint(sbase + Lay::kV + c * 16384, &p.tm_v, bar(Lay::bKV), c * 64,
+                         y0 + j * kBN, z, once);
       }
       int issued = 0;
       bool ok = true;
@@ -177,14 +202,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         const int i = i0 + t % n_head;
         const int zq = zq0 + t / n_head;
-        const size_t vrow = static_cast<size_t>(zq) * p.n_pad + static_cast<size_t>(i) * kBM;
+        const size_t vrow =
+            static_cast<size_t>(zq) * p.n_pad + static_cast<size_t>(tbase + i) * kBM;
         mbar_arrive_expect_tx(bar(Lay::bQF + s), 2 * Lay::kTile + 1024);
         #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           tma_load_3d_hint(sbase + Lay::kQ + s * Lay::kTile + c * 16384, &p.tm_q,
-                           bar(Lay::bQF + s), c * 64, i * kBM, zq, keep);
+                           bar(Lay::bQF + s), c * 64, y0 + i * kBM, zq, keep);
           tma_load_3d_hint(sbase + Lay::kDO + s * Lay::kTile + c * 16384, &p.tm_do,
-                           bar(Lay::bQF + s), c * 64, i * kBM, zq, keep);
+                           bar(Lay::bQF + s), c * 64, y0 + i * kBM, zq, keep);
         }
         bulk_load_1d(sbase + Lay::kVec + s * 1024, p.nlse2 + vrow, 512, bar(Lay::bQF + s));
         bulk_load_1d(sbase + Lay::kVec + s * 1024 + 512, p.nd + vrow, 512, bar(Lay::bQF + s));
@@ -343,8 +369,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {
       tc_fence_after();
       const int key = j * kBN + r;
-      const bool valid = key < p.N;
-      const size_t row = static_cast<size_t>(z) * p.N + (valid ? key : 0);
+      const bool valid = key < seq_len;
+      const size_t row = static_cast<size_t>(z) * p.N + y0 + (valid ? key : 0);
       bwd::store_row_half<D>(t_lane + kColDV + half * (D / 2), 1.f, p.dv + row * D + half * (D / 2),
                              valid);
       bwd::store_row_half<D>(t_lane + kColDK + half * (D / 2), p.scale,
@@ -360,7 +386,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // =================================================================================== dQ kernel
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using Lay = BwdQLayout<D>;
@@ -397,20 +423,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   // query tile i of head slice z; causal: key tiles 0..i (the heaviest tiles first), else all
-  const int BH = p.B * p.H;
   const int L = static_cast<int>(blockIdx.x);
-  int z, i;
-  if constexpr (CAUSAL) {
-    i = p.n_tiles - 1 - L / BH;
-    z = L % BH;
-  } else {  // the query tiles of a head together: its K and V tiles stay in L2
-    z = L / p.n_tiles;
-    i = L % p.n_tiles;
+  int z, i, y0 = 0, seq_len = p.N, tbase = 0;
+  if constexpr (!VARLEN) {
+    const int BH = p.B * p.H;
+    if constexpr (CAUSAL) {
+      i = p.n_tiles - 1 - L / BH;
+      z = L % BH;
+    } else {  // the query tiles of a head together: its K and V tiles stay in L2
+      z = L / p.n_tiles;
+      i = L % p.n_tiles;
+    }
+  } else {  // packed batches: z is the head, the slot blockIdx.x / H names (sequence, i)
+    z = L % p.H;
+    if (warp == 0) {
+      int start, len, tile, base;
+      bwd_locate_tile(p.cu_seqlens, p.n_seqs, p.N, L / p.H, lane, start, len, tile, base);
+      if (lane == 0) {
+        misc[2] = static_cast<uint32_t>(start);
+        misc[3] = static_cast<uint32_t>(len);
+        misc[4] = static_cast<uint32_t>(tile);
+        misc[5] = static_cast<uint32_t>(base);
+      }
+    }
   }
-  const int n_kv = CAUSAL ? i + 1 : p.n_tiles;
-  const int z_kv = (z / p.H) * p.H_kv + (z % p.H) / p.group;  // K/V head slice of query head z
-
   __syncthreads();
+  if constexpr (VARLEN) {
+    y0 = static_cast<int>(misc[2]);
+    seq_len = static_cast<int>(misc[3]);
+    i = static_cast<int>(misc[4]);
+    tbase = static_cast<int>(misc[5]);
+    if (i < 0) return;  // slot past the last tile of the batch (uniform for the CTA)
+  }
+  const int n_kv = CAUSAL ? i + 1 : (seq_len + kBN - 1) / kBN;
+  // K/V head slice of query head z
+  const int z_kv = VARLEN ? z / p.group : (z / p.H) * p.H_kv + (z % p.H) / p.group;
+
   if (warp == 1) {
     tmem_alloc(sbase + Lay::kMisc, 512);
     tmem_relinquish();
@@ -436,10 +484,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(bar(Lay::bQ), 2 * Lay::kTile);
       #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d_hint(sbase + Lay::kQ + c * 16384, &p.tm_q, bar(Lay::bQ), c * 64, i * kBM, z,
-                         once);
-        tma_load_3d_hint(sbase + Lay::kDO + c * 16384, &p.tm_do, bar(Lay::bQ), c * 64, i * kBM,
-                         z, once);
+        tma_load_3d_hint(sbase + Lay::kQ + c * 16384, &p.tm_q, bar(Lay::bQ), c * 64,
+                         y0 + i * kBM, z, once);
+        tma_load_3d_hint(sbase + Lay::kDO + c * 16384, &p.tm_do, bar(Lay::bQ), c * 64,
+                         y0 + i * kBM, z, once);
       }
       int nk = 0, nv = 0;
       bool ok = true;
@@ -453,7 +501,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kK + sk * Lay::kTile + c * 16384, &p.tm_k,
-                           bar(Lay::bKF + sk), c * 64, jj * kBN, z_kv, keep);
+                           bar(Lay::bKF + sk), c * 64, y0 + jj * kBN, z_kv, keep);
         ++nk;
         if (jj >= kBwdStages &&
             !(ok = mbar_wait(bar(Lay::bVE + sv),
@@ -463,7 +511,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d_hint(sbase + Lay::kV + sv * Lay::kTile + c * 16384, &p.tm_v,
-                           bar(Lay::bVF + sv), c * 64, jj * kBN, z_kv, keep);
+                           bar(Lay::bVF + sv), c * 64, y0 + jj * kBN, z_kv, keep);
         ++nv;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
@@ -552,8 +600,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t col_s = t_lane + kColS + 64 * half;
     const float sl2 = p.scale_log2;
-    const float nlse2 = p.nlse2[static_cast<size_t>(z) * p.n_pad + row];  // -lse * log2(e)
-    const float nd = p.nd[static_cast<size_t>(z) * p.n_pad + row];        // -D
+    const size_t prow = static_cast<size_t>(z) * p.n_pad + static_cast<size_t>(tbase) * kBM + row;
+    const float nlse2 = p.nlse2[prow];  // -lse * log2(e)
+    const float nd = p.nd[prow];        // -D
     bool ok = true;
     for (int jj = 0; jj < n_kv; ++jj) {
       const uint32_t par = static_cast<uint32_t>(jj) & 1u;
@@ -583,8 +632,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // keys past the end of the sequence, and (diagonal tile) keys after the query, get P = 0
       const int key0 = jj * kBN + 64 * half;
-      if ((CAUSAL && jj == i) || key0 + 64 > p.N) {
-        const int lim = CAUSAL ? min(p.N - key0, row - key0 + 1) : (p.N - key0);
+      if ((CAUSAL && jj == i) || key0 + 64 > seq_len) {
+        const int lim = CAUSAL ? min(seq_len - key0, row - key0 + 1) : (seq_len - key0);
         #pragma unroll
         for (int c = 0; c < 64; ++c) pf[c] = (c < lim) ? pf[c] : 0.f;
       }
@@ -621,8 +670,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           static_cast<uint32_t>((n_kv - 1) >> 1) & 1u, wc, 2, 10);
     if (ok) {
       tc_fence_after();
-      const bool valid = row < p.N;
-      const size_t grow = static_cast<size_t>(z) * p.N + (valid ? row : 0);
+      const bool valid = row < seq_len;
+      const size_t grow = static_cast<size_t>(z) * p.N + y0 + (valid ? row : 0);
       bwd::store_row_half<D>(t_lane + kColDQ + half * (D / 2), p.scale,
                              p.dq + grow * D + half * (D / 2), valid);
     }

@@ -212,3 +212,23 @@ def test_bwd_gqa_validation(lib):
     assert c(8, 3) == -3 and c(8, 0) == -3 and c(8, -2) == -3
     assert c(8, 2, d=96) == -2
     assert c(0, 0) == 0 and c(8, 2, N=0) == 0
+
+
+def test_bwd_varlen_validation(lib):
+    f = lib.attn_bwd_varlen
+    A = ALIGNED
+    big = 1 << 30
+
+    def c(cu=A, B=3, H=4, H_kv=2, T=300, d=128, ws=A, nb=big):
+        return f(A, A, A, A, A, A, A, A, A, cu, B, H, H_kv, T, d, 1, 0.1, ws, nb, None)
+
+    assert c(cu=None) == -1
+    assert c(cu=A + 2) == -4
+    assert c(H_kv=3) == -3
+    assert c(d=96) == -2
+    assert c(ws=None) == -8 and c(nb=100) == -8
+    assert c(B=0, T=5) == -3          # rows but no sequences
+    assert c(T=0) == 0
+    w = lib.attn_bwd_varlen_workspace_bytes
+    assert w(3, 4, 300, 128) == 2 * 4 * 128 * (3 + 3) * 4
+    assert w(1, 1, 1, 64) == 2 * 1024 and w(0, 1, 10, 64) == 0 and w(1, 1, 10, 96) == 0

@@ -153,3 +153,65 @@ def test_bwd_gqa(seed, B, H, H_kv, N, d, causal):
                 ak += a_k; av += a_v
             check_grad(gk[b, hk], dk[b, hk], ak, f"{w.name} dK ({b},{hk})")
             check_grad(gv[b, hk], dv[b, hk], av, f"{w.name} dV ({b},{hk})")
+
+
+def varlen_reference(q, k, v, do, cu, causal, scale):
+    """Per-sequence, per-head backward oracle on packed [H, T, d] inputs (K/V heads may be fewer)."""
+    H, T, d = q.shape
+    H_kv = k.shape[0]
+    group = H // H_kv
+    dq = np.zeros((H, T, d)); dk = np.zeros((H_kv, T, d)); dv = np.zeros((H_kv, T, d))
+    o = np.zeros((H, T, d)); lse = np.zeros((H, T))
+    bounds_q = np.zeros((H, T, d)); bounds_k = np.zeros((H_kv, T, d)); bounds_v = np.zeros((H_kv, T, d))
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b == a:
+            continue
+        for h in range(H):
+            g = h // group
+            r = bwd.attention_bwd_head(q[h, a:b], k[g, a:b], v[g, a:b], do[h, a:b], causal, scale)
+            dq[h, a:b] = r[0]; dk[g, a:b] += r[1]; dv[g, a:b] += r[2]
+            o[h, a:b] = r[3]; lse[h, a:b] = r[4]
+            qf, kf, vf, dof = (orc.bf16_bits_to_f64(x) for x in
+                               (q[h, a:b], k[g, a:b], v[g, a:b], do[h, a:b]))
+            aq, ak, av = grad_bounds(qf, kf, vf, dof, causal, scale)
+            bounds_q[h, a:b] = aq; bounds_k[g, a:b] += ak; bounds_v[g, a:b] += av
+    return (dq, dk, dv, o, lse), (bounds_q, bounds_k, bounds_v)
+
+
+@pytest.mark.parametrize("seed,lengths,H,H_kv,d,causal", [
+    (730, [1, 300, 0, 129, 640], 4, 4, 128, True),
+    (731, [256, 77, 500], 4, 2, 64, False),
+    (732, [1000], 2, 1, 128, True),
+    (733, [130, 1, 129, 128, 257], 6, 3, 128, False),
+])
+def test_bwd_varlen(seed, lengths, H, H_kv, d, causal):
+    q, k, v, cu = configs.custom_varlen(seed, lengths, H, d, causal, H_kv=H_kv)
+    T = int(cu[-1])
+    do = configs.custom(seed, 1, H, T, d, causal).make_dout()[0]   # [H, T, d]
+    scale = 1 / np.sqrt(d)
+    ref, bnd = varlen_reference(q, k, v, do, cu, causal, scale)
+    o = f64_to_bf16_dev(ref[3])
+    lse = torch.from_numpy(ref[4].astype(np.float32)).cuda()
+    cu_d = torch.from_numpy(cu).cuda()
+    g = attn.attn_bwd(to_dev(q), to_dev(k), to_dev(v), o, lse, to_dev(do), cu_seqlens=cu_d,
+                      causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    for name, x, r, b in zip(("dQ", "dK", "dV"), g, ref[:3], bnd):
+        check_grad(to_f64(x), r, b, f"varlen {lengths} {name}")
+
+
+def test_bwd_varlen_single_sequence_equals_dense():
+    w = configs.custom(734, 1, 2, 300, 128, True)
+    q, k, v, _ = w.make()
+    do = w.make_dout()
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True, scale=w.scale)
+    a = attn.attn_bwd(to_dev(q), to_dev(k), to_dev(v), o, lse, to_dev(do), causal=True,
+                      scale=w.scale)
+    cu = torch.tensor([0, 300], dtype=torch.int32, device="cuda")
+    b = attn.attn_bwd(to_dev(q[0]), to_dev(k[0]), to_dev(v[0]), o[0].contiguous(),
+                      lse[0].contiguous(), to_dev(do[0]), cu_seqlens=cu, causal=True,
+                      scale=w.scale)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):  # the same tiles in the same order: the same bits
+        assert torch.equal(x[0].view(torch.int16), y.view(torch.int16))
