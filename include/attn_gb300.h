@@ -214,8 +214,9 @@ ATTN_API int attn_quantize_fp8(const void* x, void* codes, float* scales, int B,
  * 128, dense layout.  Inputs are E4M3 codes with per-tile fp32 scales as attn_quantize_fp8
  * writes them: q8, k8 [B, H, N, 128] (transpose = 0), vt8 [B, H, 128, Npad] (transpose = 1); the
  * value of an input element is code x its tile's scale.  S = Q K^T runs on kind::f8f6f4 tensor
- * cores; the probabilities enter P V as E4M3 codes of P * 256 * sv_j / max(sv) (V's tile scales
- * folded in); O (bf16) and lse (fp32, natural log of the scaled scores' normaliser) as attn_fwd.
+ * cores; the probabilities enter P V as E4M3 codes of P * 48 * sv_j / max(sv) (V's tile scales
+ * folded in; P <= 8 against a reference maximum that trails the row maximum by at most 3 in log2
+ * units); O (bf16) and lse (fp32, natural log of the scaled scores' normaliser) as attn_fwd.
  * d other than 128: ATTN_ERR_HEAD_DIM.  Returns an attn_status.
  */
 ATTN_API int attn_fwd_fp8(const void* q8, const float* sq, const void* k8, const float* sk,

@@ -7,9 +7,9 @@
 //                        transposed, [d][keys]); 4 instructions of 32 keys
 // Tile scales enter the softmax: the scores of (query tile t, key tile j) are the raw products
 // times sq_t * sk_j * scale * log2(e).  V's tile scales are folded into the probabilities:
-// P_t V_j uses the codes of P * 256 * sv_j / sv_max, and the epilogue multiplies by
-// sv_max / (256 l).  The reference maximum trails the row maximum by at most kFp8Tau, so P <= 2^0.5
-// and the codes never saturate.  l and lse use the fp32 sums of the unrounded P.
+// P_t V_j uses the codes of P * kFp8PScale * sv_j / sv_max, and the epilogue multiplies by
+// sv_max / (kFp8PScale l).  The reference maximum trails the row maximum by at most kFp8Tau, so
+// P <= 2^kFp8Tau and the codes never saturate.  l and lse use the fp32 sums of the unrounded P.
 #pragma once
 
 #include <cuda.h>
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
       tc_fence_after();
       const float l = (le[0] + le[1]) + (le[2] + le[3]);
       const bool valid = row < seq_len;
-      const float mul = 1.f / (fv * l);  // sv_max / (256 l)
+      const float mul = 1.f / (fv * l);  // sv_max / (kFp8PScale l)
       const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
                           static_cast<size_t>(valid ? row : 0);
       uint4* orow = reinterpret_cast<uint4*>(p.o + grow * 128);
