@@ -28,8 +28,8 @@ struct FwdParams {
   int group;                 // query heads per K/V head (1: multi-head; H: multi-query)
   int n_splits;              // key-range slices per query pair (1: the whole row in one CTA)
   float* part_o;             // split-KV partials [n_splits][B H N][D] fp32 (unnormalised O)
-  float* part_stat;          // split-KV partials [3][n_splits][B H N]: reference max (log2),
-                             // exact row sum, rounded row sum
+  float* part_stat;          // split-KV partials [2][n_splits][B H N]: reference max (log2),
+                             // row sum
   int n_qt;                  // dense: query-tile pairs (256 rows) per head
   float scale_log2;          // scale * log2(e)
 };
