@@ -550,6 +550,47 @@ def run_ours(args, w, rank, world, dist):
                                       "tflops": g_flops / (g_ms * 1e-3) / 1e12}
         del dout, bws, gq, gk, gv, gqd, gkd, gvd, gdo, fo, fl
 
+    # ---- packed variable-length batch (16 sequences of U[128, 4096] rows, H=16, d=128, causal):
+    # forward and backward through the cu_seqlens entry points
+    varlen = None
+    if not args.no_extras:
+        vw = configs.WORKLOADS[5]
+        vq_np, vk_np, vv_np, vcu = vw.make()
+        vq, vk, vv = to_dev(vq_np), to_dev(vk_np), to_dev(vv_np)
+        vcu_d = torch.from_numpy(vcu).to(dev)
+        vdo = to_dev(configs.custom(vw.index, 1, vw.H, vw.total_tokens(), vw.d, True)
+                     .make_dout()[0])
+        vo, vl = attn.attn_fwd(vq, vk, vv, cu_seqlens=vcu_d, causal=True, scale=vw.scale)
+        vws = torch.empty(max(int(attn.lib().attn_bwd_varlen_workspace_bytes(
+            vw.n_seqs, vw.H, vw.total_tokens(), vw.d)), 1), dtype=torch.uint8, device=dev)
+
+        def time_it(fn, n=30):
+            for _ in range(3):
+                fn()
+            barrier()
+            evs = []
+            for _ in range(n):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                evs.append((e0, e1))
+            barrier()
+            return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+        f_ms = time_it(lambda: attn.attn_fwd(vq, vk, vv, cu_seqlens=vcu_d, causal=True,
+                                             scale=vw.scale, out=vo, lse=vl))
+        b_ms = time_it(lambda: attn.attn_bwd(vq, vk, vv, vo, vl, vdo, cu_seqlens=vcu_d,
+                                             causal=True, scale=vw.scale, workspace=vws))
+        lens = [int(x) for x in np.diff(vcu)]
+        vf = acc.attention_flops(vw.H, lens, vw.d, True)
+        varlen = {"workload": vw.name, "lengths": lens, "fwd_ms": f_ms,
+                  "fwd_tflops": vf / (f_ms * 1e-3) / 1e12, "bwd_ms": b_ms,
+                  "bwd_tflops": 2.5 * vf / (b_ms * 1e-3) / 1e12}
+        del vq, vk, vv, vo, vl, vdo, vws
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
@@ -568,7 +609,7 @@ def run_ours(args, w, rank, world, dist):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "unfused": unfused,
-            "gqa": gqa, "splitkv": splitkv, "backward": backward, "fp8": fp8,
+            "gqa": gqa, "splitkv": splitkv, "backward": backward, "fp8": fp8, "varlen": varlen,
             "clocks": clock_info, "gpu_launches": args.steps,
             "kernel_ms_median": statistics.median(per),
         }
@@ -587,7 +628,7 @@ def main():
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the grouped-query, split-KV, FP8 and backward measurements")
+                    help="skip the grouped-query, split-KV, FP8, backward and packed-batch measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
