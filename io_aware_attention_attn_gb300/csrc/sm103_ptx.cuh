@@ -79,6 +79,8 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+__device__ __forceinline__ bool lane_id_is_zero() { return (threadIdx.x & 31) == 0; }
+
 // Wait until the phase with the given parity has completed.  Returns false if `abort` is set by
 // another role or the wait exceeds kWaitLimitNs (then the status word and `abort` are set).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w,
@@ -103,6 +105,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                int role, int site) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, role, site)) != 0;
+}
+
+// Warp-uniform wait that polls with the non-suspending test instead of try_wait: for the MMA
+// issuer, whose every wait sits on the pipeline's critical chain, a suspended try_wait was seen to
+// wake a few hundred cycles after the phase completed.  Same limit and failure reporting.
+__device__ __forceinline__ bool mbar_wait_spin_warp(uint32_t bar, uint32_t parity,
+                                                    const WaitCtx& w, int role, int site) {
+  bool done = mbar_test(bar, parity);
+  if (__all_sync(0xffffffffu, done)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    #pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+    bool give_up = false;
+    if (lane_id_is_zero()) {
+      if (*w.abort) {
+        give_up = true;
+      } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicCAS(w.status, 0, kStatusTimeout | (role << 8) | (site << 16));
+        *w.abort = 1;
+        give_up = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, give_up)) return false;
+  }
 }
 
 // Drain-only wait used while unwinding after an abort: ignores the abort flag, keeps the limit.
