@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 wc, 1, 3)))
         break;
       // S^T_t rewrites the columns P^T_{t-1} was read from: wait for dV_{t-1}
-      if (t > 0 && !(ok = mbar_wait_warp(bar(Lay::bDV), par ^ 1u, wc, 1, 4))) break;
+      if (t > 0 && !(ok = mbar_wait_spin_warp(bar(Lay::bDV), par ^ 1u, wc, 1, 4))) break;
       tc_fence_after();
       if (lane == 0) {
         bwd::mma_ss_tile<D>(tmem + kColS, desc_k, desc_q + s * kTileD, kIdSS);
@@ -249,21 +249,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
       // dP^T_t rewrites the columns dS^T_{t-1} was read from: wait for dK_{t-1}
-      if (t > 0 && !(ok = mbar_wait_warp(bar(Lay::bDK), par ^ 1u, wc, 1, 5))) break;
+      if (t > 0 && !(ok = mbar_wait_spin_warp(bar(Lay::bDK), par ^ 1u, wc, 1, 5))) break;
       tc_fence_after();
       if (lane == 0) {
         bwd::mma_ss_tile<D>(tmem + kColDP, desc_v, desc_do + s * kTileD, kIdSS);
         mma_commit(bar(Lay::bDP));
       }
       __syncwarp();
-      if (!(ok = mbar_wait_warp(bar(Lay::bP), par, wc, 1, 6))) break;
+      if (!(ok = mbar_wait_spin_warp(bar(Lay::bP), par, wc, 1, 6))) break;
       tc_fence_after();
       if (lane == 0) {
         bwd::mma_ts_tile(tmem + kColDV, tmem + kColS, desc_do_mn + s * kTileD, kIdTS, t > 0);
         mma_commit(bar(Lay::bDV));
       }
       __syncwarp();
-      if (!(ok = mbar_wait_warp(bar(Lay::bDS), par, wc, 1, 7))) break;
+      if (!(ok = mbar_wait_spin_warp(bar(Lay::bDS), par, wc, 1, 7))) break;
       tc_fence_after();
       if (lane == 0) {
         bwd::mma_ts_tile(tmem + kColDK, tmem + kColDP, desc_q_mn + s * kTileD, kIdTS, t > 0);
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         return false;
       // S rewrites the columns the compute threads read S_{jj-1} from
       if (jj > 0 &&
-          !mbar_wait_warp(bar(Lay::bSR), (static_cast<uint32_t>(jj) & 1u) ^ 1u, wc, 1, 4))
+          !mbar_wait_spin_warp(bar(Lay::bSR), (static_cast<uint32_t>(jj) & 1u) ^ 1u, wc, 1, 4))
         return false;
       tc_fence_after();
       if (lane == 0) {
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           5))
         return false;
       if (jj >= 2 &&  // the buffer's previous dS was read by dQ of tile jj - 2
-          !mbar_wait_warp(bar(Lay::bDQ + b), (static_cast<uint32_t>(jj >> 1) & 1u) ^ 1u, wc, 1, 6))
+          !mbar_wait_spin_warp(bar(Lay::bDQ + b), (static_cast<uint32_t>(jj >> 1) & 1u) ^ 1u, wc, 1, 6))
         return false;
       tc_fence_after();
       if (lane == 0) {
@@ -575,8 +575,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int jj = 0; ok && jj < n_kv; ++jj) {
       const int s = jj % kBwdStagesQK, b = jj & 1;
       if (jj + 1 < n_kv && !(ok = issue_s(jj + 1) && issue_dp(jj + 1))) break;
-      if (!(ok = mbar_wait_warp(bar(Lay::bDS + b), static_cast<uint32_t>(jj >> 1) & 1u, wc, 1,
-                                7)))
+      if (!(ok = mbar_wait_spin_warp(bar(Lay::bDS + b), static_cast<uint32_t>(jj >> 1) & 1u, wc,
+                                     1, 7)))
         break;
       tc_fence_after();
       if (lane == 0) {
