@@ -43,12 +43,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 int encode_rows_map(CUtensorMap* map, const void* base, uint64_t d, uint64_t rows,
-                    uint64_t heads) {
+                    uint64_t heads, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return CUDA_ERROR_NOT_FOUND;
   const cuuint64_t dims[3] = {d, rows, heads};
   const cuuint64_t strides[2] = {d * 2, d * 2 * rows};  // bytes, dims 1 and 2
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -148,10 +148,13 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if ((rc = check_device()) != 0) return rc;
   FwdParams p{};
   const bool varlen = cu_seqlens != nullptr;
+  // dense head dim 128 in one pass over the keys runs on CTA pairs (one query tile per SM, each
+  // SM loading 64-key halves of the K tiles); everything else on the two-tile kernel
+  const bool two_sm = d == 128 && !varlen && n_splits == 1;
   const uint64_t q_heads = varlen ? static_cast<uint64_t>(H) : static_cast<uint64_t>(B) * H;
   const uint64_t kv_heads = varlen ? static_cast<uint64_t>(Hkv) : static_cast<uint64_t>(B) * Hkv;
   if (encode_rows_map(&p.tm_q, q, d, N, q_heads) != CUDA_SUCCESS ||
-      encode_rows_map(&p.tm_k, k, d, N, kv_heads) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_k, k, d, N, kv_heads, two_sm ? 64u : 128u) != CUDA_SUCCESS ||
       encode_rows_map(&p.tm_v, v, d, N, kv_heads) != CUDA_SUCCESS)
     return ATTN_ERR_LAUNCH;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -169,11 +172,14 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.n_qt = (N + 2 * kBM - 1) / (2 * kBM);  // pairs of 128-row query tiles per head
   p.scale_log2 = scale * 1.4426950408889634f;
   const long long grid = varlen ? static_cast<long long>(p.n_qt + B) * H
-                                 : static_cast<long long>(p.n_qt) * B * H * n_splits;
+                                 : static_cast<long long>(p.n_qt) * B * H * n_splits *
+                                       (two_sm ? 2 : 1);
   if (grid > INT_MAX) return ATTN_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, static_cast<int>(grid), st)
-                            : launch_fwd_d128(p, causal != 0, varlen, static_cast<int>(grid), st);
+  cudaError_t e =
+      two_sm    ? launch_fwd_d128_2sm(p, causal != 0, static_cast<int>(grid), st)
+      : (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, static_cast<int>(grid), st)
+                  : launch_fwd_d128(p, causal != 0, varlen, static_cast<int>(grid), st);
   if (e == cudaSuccess && n_splits > 1)
     e = launch_splitkv_combine(d, part_o, part_stat, o, lse, static_cast<long long>(B) * H * N,
                                n_splits, st);

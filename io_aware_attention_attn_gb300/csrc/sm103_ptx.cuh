@@ -133,6 +133,36 @@ __device__ __forceinline__ bool mbar_wait_spin_warp(uint32_t bar, uint32_t parit
   }
 }
 
+// Warp-uniform wait in which only lane 0 polls (with the non-suspending test) and the other
+// lanes take its answer: the polling warp then takes one issue slot per test instead of 32 lanes'
+// worth of shared-memory requests.  Same limit and failure reporting.
+__device__ __forceinline__ bool mbar_wait_spin_lane0(uint32_t bar, uint32_t parity,
+                                                     const WaitCtx& w, int role, int site) {
+  int state = 0;  // 1 done, 2 gave up
+  if (lane_id_is_zero()) {
+    if (mbar_test(bar, parity)) {
+      state = 1;
+    } else {
+      const unsigned long long t0 = global_timer_ns();
+      for (;;) {
+        #pragma unroll 1
+        for (int i = 0; i < 256 && state == 0; ++i)
+          if (mbar_test(bar, parity)) state = 1;
+        if (state) break;
+        if (*w.abort) {
+          state = 2;
+        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicCAS(w.status, 0, kStatusTimeout | (role << 8) | (site << 16));
+          *w.abort = 1;
+          state = 2;
+        }
+        if (state) break;
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, state, 0) == 1;
+}
+
 // Drain-only wait used while unwinding after an abort: ignores the abort flag, keeps the limit.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = global_timer_ns();
@@ -483,6 +513,97 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+
+// ------------------------------------------------------------------ two-SM (CTA pair) forms
+// A cluster of two CTAs on the two SMs of a TPC can run one tcgen05 MMA across both SMs
+// (cta_group::2): the even-ranked CTA issues it, each CTA supplies half of the M rows of A and
+// half of the N columns of B from its own shared memory, and each CTA's tensor memory receives
+// its own M/2 rows of D.  Every tcgen05 allocation, MMA and commit of such a kernel uses
+// cta_group::2.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address, in the cluster's shared window, of the variable at local shared address `addr` in the
+// CTA of rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its cluster-window address (it may sit in the peer CTA).  The
+// default (CTA-scope release) semantics: the data this arrival publishes lives in tensor memory and
+// is ordered by tcgen05.wait::st and tcgen05.fence::before_thread_sync on the arriving side and
+// tcgen05.fence::after_thread_sync on the waiting side; a cluster-scope release would add a
+// memory barrier to every arrival.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Whole-cluster barrier (every thread of both CTAs), release / acquire.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 3-D tiled load into this CTA's shared memory whose completion is signalled on a barrier that
+// may sit in the peer CTA (`bar_cluster`: cluster-window address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
+                                                 uint32_t bar_cluster, int x, int y, int z,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z),
+      "l"(policy)
+      : "memory");
+}
+
+// Collective over one warp of each CTA of the pair.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on the barrier at local address `bar` in every CTA of `cta_mask` when all
+// cta_group::2 MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 }  // namespace attn
