@@ -398,8 +398,8 @@ def run_ours(args, w, rank, world, dist):
                "kv_bytes_saved": 2 * (g.H - g.kv_heads) * g.B * g.N * g.d * 2}
         del gq, gk, gv, go, gl
 
-    # ---- split-KV on a few-heads, long-sequence shape (64 query pairs for 152 SMs): the
-    # library's slice count against one slice (the plain fused kernel)
+    # ---- split-KV on a few-heads, long-sequence shape (32 query pairs, 64 of the 152 SMs in one
+    # slice): the library's slice count against one slice (the plain fused kernel)
     splitkv = None
     if not args.no_extras:
         sw = configs.SPLITKV
@@ -431,7 +431,7 @@ def run_ours(args, w, rank, world, dist):
 
         ms_auto = time_split(0)
         ms_one = time_split(1)
-        chosen = attn.splitkv_slices(sw.B, sw.H, sw.N, 0)
+        chosen = attn.splitkv_slices(sw.B, sw.H, sw.N, sw.d, 0)
         splitkv = {"workload": sw.name, "splits": chosen, "ms": ms_auto,
                    "tflops": s_flops / (ms_auto * 1e-3) / 1e12, "ms_one_slice": ms_one,
                    "tflops_one_slice": s_flops / (ms_one * 1e-3) / 1e12,

@@ -114,9 +114,9 @@ HEADLINE = 3
 # Grouped-query variant of the headline shape (32 query heads sharing 8 K/V heads).
 GQA = Workload(6, "B2-H32-KV8-N4096-d128", B=2, H=32, N=4096, d=128, causal=False, H_kv=8)
 
-# Few heads, long sequence: 64 query pairs leave most of the 152 SMs idle unless the key range
-# is split (the split-KV case).
-SPLITKV = Workload(7, "B1-H2-N8192-d128", B=1, H=2, N=8192, d=128, causal=False)
+# Few heads, long sequence: 32 query pairs (64 SMs at head dim 128) leave most of the 152 SMs
+# idle unless the key range is split (the split-KV case).
+SPLITKV = Workload(7, "B1-H1-N8192-d128", B=1, H=1, N=8192, d=128, causal=False)
 
 
 def custom(index_seed: int, B: int, H: int, N: int, d: int, causal: bool,

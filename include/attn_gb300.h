@@ -98,8 +98,8 @@ ATTN_API int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
 
 /*
  * Split-KV forward for problems with few query tiles (small B * H): the key/value sequence of
- * every pair of query tiles is cut into num_splits contiguous slices, one CTA per slice, so that
- * more SMs share the work (sequence-dimension parallelism, CS336 Lecture 5 notes, section 6.3).
+ * every pair of query tiles is cut into num_splits contiguous slices, each computed by its own
+ * CTA (head dim 64) or cluster of two CTAs (head dim 128), so that more SMs share the work (sequence-dimension parallelism, CS336 Lecture 5 notes, section 6.3).
  * Each slice leaves its unnormalised output, its reference row maximum and its row sums in
  * `workspace`; a second kernel on `stream` merges the slices with the block merge of the CS336
  * GPU/attention notes, "Online softmax 回顾" (M = max of the slice maxima, each slice weighted by
@@ -107,7 +107,8 @@ ATTN_API int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
  * Dense layout only: q, k, v, o [B, H, N, d] bf16, lse [B, H, N] fp32, as attn_fwd.
  *   num_splits : slices per query pair, at most 32 and at most the number of 128-key tiles
  *                (larger values are lowered).  <= 0 lets the library choose: the count that
- *                minimises (waves of 152 CTAs) x (key tiles per slice + 2), the smallest on ties.
+ *                minimises (waves of units) x (key tiles per slice + 2), the smallest on ties,
+ *                where a wave is 152 units at d = 64 and 76 (two SMs each) at d = 128.
  *                When the count is 1 this is attn_fwd and the workspace is not touched.
  *   workspace  : caller-owned device buffer of at least
  *                attn_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) bytes, 256-byte
@@ -119,9 +120,10 @@ ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void*
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * The slice count attn_fwd_splitkv uses for these sizes and num_splits (0 for invalid sizes).
+ * The slice count attn_fwd_splitkv uses for these sizes and num_splits (0 for invalid sizes or
+ * a head dim other than 64 and 128).
  */
-ATTN_API int attn_fwd_splitkv_slices(int B, int H, int N, int num_splits);
+ATTN_API int attn_fwd_splitkv_slices(int B, int H, int N, int d, int num_splits);
 
 /*
  * Workspace bytes attn_fwd_splitkv needs: with S the slice count it will use, an fp32 partial

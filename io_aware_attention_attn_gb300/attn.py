@@ -29,7 +29,7 @@ SIGNATURES = {
     "attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "attn_fwd_splitkv_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
-    "attn_fwd_splitkv_slices": (_I, [_I, _I, _I, _I]),
+    "attn_fwd_splitkv_slices": (_I, [_I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
     "attn_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                           _S, _P]),
@@ -152,8 +152,8 @@ def splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int = 0)
     return int(lib().attn_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits))
 
 
-def splitkv_slices(B: int, H: int, N: int, num_splits: int = 0) -> int:
-    return int(lib().attn_fwd_splitkv_slices(B, H, N, num_splits))
+def splitkv_slices(B: int, H: int, N: int, d: int, num_splits: int = 0) -> int:
+    return int(lib().attn_fwd_splitkv_slices(B, H, N, d, num_splits))
 
 
 def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,

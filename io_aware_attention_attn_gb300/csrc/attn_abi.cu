@@ -148,9 +148,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if ((rc = check_device()) != 0) return rc;
   FwdParams p{};
   const bool varlen = cu_seqlens != nullptr;
-  // dense head dim 128 in one pass over the keys runs on CTA pairs (one query tile per SM, each
-  // SM loading 64-key halves of the K tiles); everything else on the two-tile kernel
-  const bool two_sm = d == 128 && !varlen && n_splits == 1;
+  // dense head dim 128 runs on CTA pairs (one query tile per SM, each SM loading 64-key halves of
+  // the K tiles), split-KV slices included; head dim 64 and packed batches on the two-tile kernel
+  const bool two_sm = d == 128 && !varlen;
   const uint64_t q_heads = varlen ? static_cast<uint64_t>(H) : static_cast<uint64_t>(B) * H;
   const uint64_t kv_heads = varlen ? static_cast<uint64_t>(Hkv) : static_cast<uint64_t>(B) * Hkv;
   if (encode_rows_map(&p.tm_q, q, d, N, q_heads) != CUDA_SUCCESS ||
@@ -209,14 +209,14 @@ extern "C" int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o
   return fwd_impl(q, k, v, o, lse, cu_seqlens, B, H, H_kv, N, d, causal, scale, stream);
 }
 
-extern "C" int attn_fwd_splitkv_slices(int B, int H, int N, int num_splits) {
-  if (B <= 0 || H <= 0 || N <= 0) return 0;
-  return splitkv_pick(B, H, N, num_splits);
+extern "C" int attn_fwd_splitkv_slices(int B, int H, int N, int d, int num_splits) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  return splitkv_pick(B, H, N, d, num_splits);
 }
 
 extern "C" size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
   if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
-  const int S = splitkv_pick(B, H, N, num_splits);
+  const int S = splitkv_pick(B, H, N, d, num_splits);
   return S > 1 ? splitkv_bytes(B, H, N, d, S) : 0;
 }
 
@@ -227,7 +227,7 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
   bool empty = false;
   const int rc = validate(q, k, v, o, lse, nullptr, B, H, N, d, scale, &empty);
   if (rc != ATTN_OK || empty) return rc;
-  const int S = splitkv_pick(B, H, N, num_splits);
+  const int S = splitkv_pick(B, H, N, d, num_splits);
   if (S == 1) return fwd_impl(q, k, v, o, lse, nullptr, B, H, H, N, d, causal, scale, stream);
   const size_t need = splitkv_bytes(B, H, N, d, S);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)

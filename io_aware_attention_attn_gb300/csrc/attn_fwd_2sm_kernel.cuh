@@ -84,6 +84,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // ---- the 256 query rows of this cluster: z = head slice of the tensor maps, pt = row pair;
+  // with split-KV, consecutive clusters are the key slices of one row pair
+  const int BH = p.B * p.H;
+  const int L = (static_cast<int>(blockIdx.x) >> 1) / p.n_splits;
+  const int split = (static_cast<int>(blockIdx.x) >> 1) % p.n_splits;
+  int z, pt;
+  if constexpr (CAUSAL) {  // heaviest pairs (most key tiles) first
+    pt = p.n_qt - 1 - L / BH;
+    z = L % BH;
+  } else {                 // all pairs of a head together: its K and V stay in L2
+    z = L / p.n_qt;
+    pt = L % p.n_qt;
+  }
+  const int seq_len = p.N;
+  const int n_keytiles = (seq_len + kBN - 1) / kBN;
+  // key tiles of the row pair (causal: up to the diagonal of its last row); both CTAs run the
+  // same count, rank 0's rows of a tile past their diagonal are fully masked.  This cluster takes
+  // key tiles [kb, kb + n) of them; pipeline bookkeeping runs over j = 0..n-1, key tile kb + j is
+  // the data.
+  const int n_full = CAUSAL ? min(n_keytiles, 2 * pt + 2) : n_keytiles;
+  const int chunk = (n_full + p.n_splits - 1) / p.n_splits;
+  const int kb = split * chunk;
+  const int n = max(0, min(kb + chunk, n_full) - kb);
+  const int qrow0 = (2 * pt + static_cast<int>(rank)) * kBM;  // first row of this CTA's tile
+  const int z_kv = (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
+  if (n == 0) {
+    // a key slice past the end of this pair's range (uniform for the cluster, before any
+    // cluster-wide step): the merge reads max -inf and sum 0 for these rows
+    const size_t rows_total = static_cast<size_t>(p.B) * p.H * p.N;
+    const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
+    const int row = qrow0 + static_cast<int>(threadIdx.x);
+    if (threadIdx.x < kBM && row < seq_len) {
+      const size_t slot = static_cast<size_t>(split) * rows_total +
+                          static_cast<size_t>(z) * static_cast<size_t>(p.N) + row;
+      p.part_stat[slot] = -INFINITY;
+      p.part_stat[plane + slot] = 0.f;
+    }
+    return;
+  }
+
   if (threadIdx.x == 0) {
     mbar_init(bar(Lay::bQ), 1);
     for (int s = 0; s < SK; ++s) {
@@ -114,25 +154,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  // ---- the 256 query rows of this cluster: z = head slice of the tensor maps, pt = row pair
-  const int BH = p.B * p.H;
-  const int L = static_cast<int>(blockIdx.x) >> 1;
-  int z, pt;
-  if constexpr (CAUSAL) {  // heaviest pairs (most key tiles) first
-    pt = p.n_qt - 1 - L / BH;
-    z = L % BH;
-  } else {                 // all pairs of a head together: its K and V stay in L2
-    z = L / p.n_qt;
-    pt = L % p.n_qt;
-  }
-  const int seq_len = p.N;
-  const int n_keytiles = (seq_len + kBN - 1) / kBN;
-  // key tiles the cluster visits (causal: up to the diagonal of its last row); both CTAs run the
-  // same count, rank 0's rows of a tile past their diagonal are fully masked
-  const int n = CAUSAL ? min(n_keytiles, 2 * pt + 2) : n_keytiles;
-  const int qrow0 = (2 * pt + static_cast<int>(rank)) * kBM;  // first row of this CTA's tile
-  const int z_kv = (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
-
   if (warp == 0) {
     // ===================================================================== TMA producer
     if (lane == 0) {
@@ -158,8 +179,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
         #pragma unroll
         for (int c = 0; c < 2; ++c)
           tma_load_3d_pair(sbase + Lay::kK + sk * Lay::kKBytes + c * 8192, &p.tm_k,
-                           lbar(Lay::bKF + sk), c * 64, j * kBN + 64 * static_cast<int>(rank),
-                           z_kv, keep);
+                           lbar(Lay::bKF + sk), c * 64,
+                           (kb + j) * kBN + 64 * static_cast<int>(rank), z_kv, keep);
         ++nk;
         if (j >= SV &&
             !(ok = mbar_wait(bar(Lay::bVE + sv), (static_cast<uint32_t>(j / SV) & 1u) ^ 1u, wc,
@@ -167,7 +188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           break;
         if (leader) mbar_arrive_expect_tx(bar(Lay::bVF + sv), 2 * Lay::kVBytes);
         tma_load_3d_pair(sbase + Lay::kV + sv * Lay::kVBytes, &p.tm_v, lbar(Lay::bVF + sv),
-                         64 * static_cast<int>(rank), j * kBN, z_kv, keep);
+                         64 * static_cast<int>(rank), (kb + j) * kBN, z_kv, keep);
         ++nv;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the cluster exits
@@ -290,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
         s[64 + i] = u2f(u2[i]);
         s[96 + i] = u2f(u3[i]);
       }
-      const int key0 = j * kBN;
+      const int key0 = (kb + j) * kBN;
       if ((CAUSAL && key0 + kBN - 1 > qrow0) || key0 + kBN > seq_len) {
         const int lim = CAUSAL ? min(seq_len - key0, row - key0 + 1) : (seq_len - key0);
         #pragma unroll
@@ -375,12 +396,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lbar(Lay::bPF + b));
     }
-    if (n > 0 && ok) ok = mbar_wait_warp(bar(Lay::bOD), 0, wc, 2, 10);
+    if (ok) ok = mbar_wait_warp(bar(Lay::bOD), 0, wc, 2, 10);
     const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
     const bool valid = row < seq_len;
     const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
                         static_cast<size_t>(row);
-    if (n > 0 && ok) {
+    if (p.n_splits > 1) {
+      // this key slice's partial result for the merge: unnormalised O, reference max and row sum
+      const size_t rows_total = static_cast<size_t>(p.B) * p.H * p.N;
+      const size_t slot = static_cast<size_t>(split) * rows_total + grow;
+      const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
+      if (valid) {
+        p.part_stat[slot] = ok ? m2 : -INFINITY;
+        p.part_stat[plane + slot] = ok ? l_exact : 0.f;
+      }
+      if (ok) {
+        tc_fence_after();
+        float4* prow = reinterpret_cast<float4*>(p.part_o + slot * D);
+        #pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_col + c * 32, o);
+          tmem_wait_ld_regs(o);
+          if (valid) {
+            #pragma unroll
+            for (int q = 0; q < 8; ++q)
+              prow[c * 8 + q] = make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]),
+                                            u2f(o[4 * q + 3]));
+          }
+        }
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l_exact;
       uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);

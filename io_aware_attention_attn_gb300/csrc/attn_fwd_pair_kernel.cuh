@@ -187,7 +187,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                           static_cast<size_t>(z) * static_cast<size_t>(p.N) + row;
       p.part_stat[slot] = -INFINITY;
       p.part_stat[plane + slot] = 0.f;
-      p.part_stat[2 * plane + slot] = 0.f;
     }
     return;
   }

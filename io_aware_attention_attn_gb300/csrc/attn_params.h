@@ -104,16 +104,20 @@ cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, bool varlen, int gri
                            cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, bool varlen, int grid,
                             cudaStream_t stream);
-// Dense head dim 128 on CTA pairs: `grid` = 2 x query pairs; p.tm_k has a 64-row box.
+// Dense head dim 128 on CTA pairs: `grid` = 2 x query pairs x key slices; p.tm_k has a 64-row
+// box.
 cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, int grid, cudaStream_t stream);
 
 // Split-KV: slices per query pair the library picks when the caller passes num_splits <= 0, and
 // the merge of the slices' partial results (attn_splitkv.cu).  The pick minimises a simple cost
-// model of the launch: waves of one-CTA-per-SM work (152 SMs) times the key tiles one slice
-// visits plus about two tiles of fixed per-CTA cost (prologue, epilogue, partial write-out).
+// model of the launch: waves of (query pair, slice) units times the key tiles one slice visits
+// plus about two tiles of fixed per-unit cost (prologue, epilogue, partial write-out).  A unit is
+// one CTA on one SM at head dim 64 (152 at once) and a cluster of two CTAs on two SMs at head dim
+// 128 (76 at once).
 constexpr int kSmCount = 152;
 constexpr int kMaxSplits = 32;
-inline int splitkv_pick(int B, int H, int N, int num_splits) {
+inline int splitkv_pick(int B, int H, int N, int d, int num_splits) {
+  const long long slots = d == 128 ? kSmCount / 2 : kSmCount;
   const long long pairs = static_cast<long long>((N + 2 * kBM - 1) / (2 * kBM)) * B * H;
   const int key_tiles = (N + kBN - 1) / kBN;
   const int cap = key_tiles < kMaxSplits ? key_tiles : kMaxSplits;
@@ -122,7 +126,7 @@ inline int splitkv_pick(int B, int H, int N, int num_splits) {
   int best = 1;
   long long best_cost = -1;
   for (int s = 1; s <= cap; ++s) {
-    const long long waves = (pairs * s + kSmCount - 1) / kSmCount;
+    const long long waves = (pairs * s + slots - 1) / slots;
     const long long cost = waves * ((key_tiles + s - 1) / s + 2);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;

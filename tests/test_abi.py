@@ -111,11 +111,14 @@ def test_gqa_validation(lib):
 
 def test_splitkv_workspace_bytes(lib):
     f = lib.attn_fwd_splitkv_workspace_bytes
-    # B=1, H=2, N=8192: 64 query pairs over 64 key tiles; cost(1) = 66, cost(2) = 1 wave x 34,
-    # cost(3) = 2 waves x 24 -> 2 slices
-    rows = 1 * 2 * 8192
-    assert f(1, 2, 8192, 128, 0) == 2 * rows * 128 * 4 + 2 * 2 * rows * 4
-    # B=1, H=1, N=16384: 64 pairs, 128 key tiles; 7 slices (3 waves x 21) beat 2 (1 x 66)
+    # head dim 128: a unit is a cluster on two SMs, 76 at once.  B=1, H=1, N=8192: 32 query pairs
+    # over 64 key tiles; cost(1) = 66, cost(2) = 1 wave x 34, cost(3) = 2 waves x 24 -> 2 slices
+    rows = 8192
+    assert f(1, 1, 8192, 128, 0) == 2 * rows * 128 * 4 + 2 * 2 * rows * 4
+    # B=1, H=2, N=8192 already fills 128 SMs in one slice: cost(1) = 66 < cost(2) = 2 x 34
+    assert f(1, 2, 8192, 128, 0) == 0
+    # head dim 64: one CTA per unit, 152 at once.  B=1, H=1, N=16384: 64 pairs, 128 key tiles;
+    # 7 slices (3 waves x 21) beat 2 (1 x 66)
     rows = 16384
     assert f(1, 1, 16384, 64, 0) == 7 * rows * 64 * 4 + 2 * 7 * rows * 4
     assert f(1, 2, 8192, 128, 5) == 5 * 2 * 8192 * 128 * 4 + 2 * 5 * 2 * 8192 * 4
@@ -124,7 +127,7 @@ def test_splitkv_workspace_bytes(lib):
     o_bytes = -(-8 * rows * 64 * 4 // 256) * 256
     assert f(1, 1, 1000, 64, 100) == o_bytes + -(-2 * 8 * rows * 4 // 256) * 256
     assert f(1, 1, 1 << 20, 64, 1000) == 32 * (1 << 20) * 64 * 4 + 2 * 32 * (1 << 20) * 4
-    assert f(1, 2, 8192, 128, 1) == 0        # one slice: plain fused forward, no workspace
+    assert f(1, 1, 8192, 128, 1) == 0        # one slice: plain fused forward, no workspace
     assert f(2, 32, 4096, 128, 0) == 0       # 1024 pairs already fill the GPU
     assert f(1, 1, 100, 64, 4) == 0          # a single key tile cannot be split
     assert f(1, 1, 1000, 96, 2) == 0
@@ -133,10 +136,12 @@ def test_splitkv_workspace_bytes(lib):
 
 def test_splitkv_slices(lib):
     f = lib.attn_fwd_splitkv_slices
-    assert f(1, 2, 8192, 0) == 2 and f(1, 1, 16384, 0) == 7 and f(2, 32, 4096, 0) == 1
-    assert f(1, 1, 1000, 0) == 8 and f(1, 1, 1000, 3) == 3 and f(1, 1, 1000, 50) == 8
-    assert f(1, 1, 1 << 20, 1000) == 32 and f(1, 1, 100, 0) == 1
-    assert f(0, 1, 100, 0) == 0 and f(1, 1, -5, 0) == 0
+    assert f(1, 1, 8192, 128, 0) == 2 and f(1, 2, 8192, 128, 0) == 1
+    assert f(1, 2, 8192, 64, 0) == 2 and f(1, 1, 16384, 64, 0) == 7
+    assert f(2, 32, 4096, 128, 0) == 1
+    assert f(1, 1, 1000, 64, 0) == 8 and f(1, 1, 1000, 64, 3) == 3 and f(1, 1, 1000, 64, 50) == 8
+    assert f(1, 1, 1 << 20, 64, 1000) == 32 and f(1, 1, 100, 64, 0) == 1
+    assert f(0, 1, 100, 64, 0) == 0 and f(1, 1, -5, 64, 0) == 0 and f(1, 1, 1000, 96, 0) == 0
 
 
 def test_splitkv_validation(lib):

@@ -70,7 +70,7 @@ def test_splitkv_full_size_sampled():
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, w.N - 1],
                                      rng.integers(0, w.N, 80)]))
     go, gl, ro, rl = [], [], [], []
-    for b, h in [(0, 0), (0, 1)]:
+    for b, h in [(bb, hh) for bb in range(w.B) for hh in range(w.H)]:
         a, c = orc.attention_head_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
         go.append(o[b, h, rows]); gl.append(lse[b, h, rows]); ro.append(a); rl.append(c)
     check(np.concatenate(go), np.concatenate(gl), np.concatenate(ro), np.concatenate(rl), w.name)
