@@ -216,12 +216,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
         const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);
         const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
         for (int j = 0; ok && j < n; ++j) {
-          if (j >= NB && !(ok = mbar_wait_spin_lane0(bar(Lay::bPV + j % NB),
-                                                     static_cast<uint32_t>((j - NB) / NB) & 1u,
-                                                     wc, 1, 7)))
+          // the S issuer runs ahead of the softmax: its waits may suspend (spinning here took
+          // issue slots from the softmax warp on the same sub-partition)
+          if (j >= NB && !(ok = mbar_wait_warp(bar(Lay::bPV + j % NB),
+                                               static_cast<uint32_t>((j - NB) / NB) & 1u, wc, 1,
+                                               7)))
             break;
-          if (!(ok = mbar_wait_spin_lane0(bar(Lay::bKF + j % SK),
-                                          static_cast<uint32_t>(j / SK) & 1u, wc, 1, 3)))
+          if (!(ok = mbar_wait_warp(bar(Lay::bKF + j % SK), static_cast<uint32_t>(j / SK) & 1u,
+                                    wc, 1, 3)))
             break;
           tc_fence_after();
           if (lane == 0) {
