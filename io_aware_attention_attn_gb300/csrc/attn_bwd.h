@@ -22,7 +22,7 @@
 
 namespace attn {
 
-constexpr int kBwdThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 two column halves
+constexpr int kBwdThreads = 352;  // warp 0 TMA, warps 1 and 10 MMA, warps 2..9 column halves
 constexpr int kBwdStages = 2;     // depth of the streamed-tile rings
 
 struct BwdParams {
@@ -61,15 +61,15 @@ struct BwdKvLayout {
   enum {
     bKV = 0,                  // K_j and V_j landed
     bQF = 1,                  // Q_i, dO_i and vectors landed [kBwdStages]
-    bQE = bQF + kBwdStages,   // stage free                   [kBwdStages]
+    bQE = bQF + kBwdStages,   // stage free (both issuers)    [kBwdStages]
     bS = bQE + kBwdStages,    // S^T = K Q^T written
     bDP,                      // dP^T = V dO^T written
     bP,                       // P^T (bf16) written over S^T (256 arrivals)
     bDS,                      // dS^T (bf16) written over dP^T (256 arrivals)
     bDV,                      // dV += P^T dO completed
-    bDK,                      // dK += dS^T Q completed (and every earlier MMA)
-    bDR,                      // drain after an abort
-    kNumBars
+    bDK,                      // dK += dS^T Q completed
+    bDR,                      // drain after an abort, one per issuer [2]
+    kNumBars = bDR + 2
   };
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..5] tile
   static constexpr int kBytes = kMisc + 32;
@@ -90,7 +90,7 @@ struct BwdQLayout {
   enum {
     bQ = 0,                   // Q_i and dO_i landed
     bKF = 1,                  // K stage full [kBwdStagesQK]
-    bKE = bKF + kBwdStagesQK, // K stage free [kBwdStagesQK]
+    bKE = bKF + kBwdStagesQK, // K stage free (both issuers) [kBwdStagesQK]
     bVF = bKE + kBwdStagesQK, // V stage full [kBwdStages]
     bVE = bVF + kBwdStages,   // V stage free [kBwdStages]
     bS = bVE + kBwdStages,    // S = Q K^T written
@@ -98,8 +98,8 @@ struct BwdQLayout {
     bDP,                      // dP = dO V^T written            [2 tensor-memory buffers]
     bDS = bDP + 2,            // dS (bf16) written over dP       [2] (256 arrivals)
     bDQ = bDS + 2,            // dQ += dS K from buffer completed [2]
-    bDR = bDQ + 2,            // drain after an abort
-    kNumBars
+    bDR = bDQ + 2,            // drain after an abort, one per issuer [2]
+    kNumBars = bDR + 2
   };
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..5] tile
   static constexpr int kBytes = kMisc + 32;

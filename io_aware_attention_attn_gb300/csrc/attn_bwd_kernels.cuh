@@ -4,8 +4,11 @@
 // TMA-fed shared-memory rings, and rebuild P from the saved logsumexp instead of reading any
 // N x N matrix (CS336 Lecture 5 notes, section 6.2, "反向传播怎么办").
 //
-// Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA issuer (lane 0);
-// warps 2..9 compute.  A compute thread owns one row of the resident tile (its TMEM lane: warp
+// Warp roles (352 threads): warp 0 TMA producer; warp 1 TMEM owner and an MMA issuer (lane 0);
+// warp 10 the second MMA issuer; warps 2..9 compute.  Each kernel's products form two chains
+// that only meet through the compute warps (dK/dV: S^T -> dV and dP^T -> dK; dQ: S and dP, then
+// dQ), one per issuing thread: an MMA issue blocks until the tensor pipe accepts it, so one
+// thread issuing both chains left the pipe idle during each of its waits.  A compute thread owns one row of the resident tile (its TMEM lane: warp
 // w may access lanes 32*(w%4)..+31) and one half of the streamed tile's 128 columns: warps 2..5
 // take columns 0..63, warps 6..9 columns 64..127.
 //
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(Lay::bKV), 1);
     for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(bar(Lay::bQF + s), 1);
-      mbar_init(bar(Lay::bQE + s), 1);
+      mbar_init(bar(Lay::bQE + s), 2);  // a commit of each issuer
     }
     mbar_init(bar(Lay::bS), 1);
     mbar_init(bar(Lay::bDP), 1);
@@ -115,6 +118,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(Lay::bDV), 1);
     mbar_init(bar(Lay::bDK), 1);
     mbar_init(bar(Lay::bDR), 1);
+    mbar_init(bar(Lay::bDR + 1), 1);
     fence_barrier_init();
     misc[1] = 0;
   }
@@ -223,16 +227,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           static_cast<uint32_t>(t / kBwdStages) & 1u);
       }
     }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
+  } else if (warp == 1 || warp == 10) {
+    // ============================ MMA issuers: S^T and dV on warp 1, dP^T and dK on warp 10
     constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
-    const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
-    const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16, 1024);
-    const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);         // K-major use
-    const uint64_t desc_do = sdesc_sw128(sbase + Lay::kDO, 16, 1024);
-    const uint64_t desc_q_mn = sdesc_sw128(sbase + Lay::kQ, 16384, 1024);   // MN-major use
-    const uint64_t desc_do_mn = sdesc_sw128(sbase + Lay::kDO, 16384, 1024);
+    const bool chain_s = warp == 1;
+    const uint64_t desc_a = sdesc_sw128(sbase + (chain_s ? Lay::kK : Lay::kV), 16, 1024);
+    const uint64_t desc_b = sdesc_sw128(sbase + (chain_s ? Lay::kQ : Lay::kDO), 16, 1024);
+    // dV reads dO and dK reads Q, both MN-major
+    const uint64_t desc_mn = sdesc_sw128(sbase + (chain_s ? Lay::kDO : Lay::kQ), 16384, 1024);
+    const uint32_t col_ss = chain_s ? kColS : kColDP;
+    const uint32_t col_acc = chain_s ? kColDV : kColDK;
+    const int b_ss = chain_s ? Lay::bS : Lay::bDP;         // SS product written
+    const int b_in = chain_s ? Lay::bP : Lay::bDS;         // its bf16 rewrite by the compute
+    const int b_acc = chain_s ? Lay::bDV : Lay::bDK;       // the TS product completed
     bool ok = mbar_wait_warp(bar(Lay::bKV), 0, wc, 1, 2);
     for (int t = 0; ok && t < n_it; ++t) {
       const int s = t % kBwdStages;
@@ -240,42 +248,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!(ok = mbar_wait_warp(bar(Lay::bQF + s), static_cast<uint32_t>(t / kBwdStages) & 1u,
                                 wc, 1, 3)))
         break;
-      // S^T_t rewrites the columns P^T_{t-1} was read from: wait for dV_{t-1}
-      if (t > 0 && !(ok = mbar_wait_spin_warp(bar(Lay::bDV), par ^ 1u, wc, 1, 4))) break;
+      // the SS product rewrites the columns the previous TS product read its A operand from
+      if (t > 0 && !(ok = mbar_wait_spin_warp(bar(b_acc), par ^ 1u, wc, 1, chain_s ? 4 : 5)))
+        break;
       tc_fence_after();
       if (lane == 0) {
-        bwd::mma_ss_tile<D>(tmem + kColS, desc_k, desc_q + s * kTileD, kIdSS);
-        mma_commit(bar(Lay::bS));
+        bwd::mma_ss_tile<D>(tmem + col_ss, desc_a, desc_b + s * kTileD, kIdSS);
+        mma_commit(bar(b_ss));
       }
       __syncwarp();
-      // dP^T_t rewrites the columns dS^T_{t-1} was read from: wait for dK_{t-1}
-      if (t > 0 && !(ok = mbar_wait_spin_warp(bar(Lay::bDK), par ^ 1u, wc, 1, 5))) break;
+      if (!(ok = mbar_wait_spin_warp(bar(b_in), par, wc, 1, chain_s ? 6 : 7))) break;
       tc_fence_after();
       if (lane == 0) {
-        bwd::mma_ss_tile<D>(tmem + kColDP, desc_v, desc_do + s * kTileD, kIdSS);
-        mma_commit(bar(Lay::bDP));
-      }
-      __syncwarp();
-      if (!(ok = mbar_wait_spin_warp(bar(Lay::bP), par, wc, 1, 6))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        bwd::mma_ts_tile(tmem + kColDV, tmem + kColS, desc_do_mn + s * kTileD, kIdTS, t > 0);
-        mma_commit(bar(Lay::bDV));
-      }
-      __syncwarp();
-      if (!(ok = mbar_wait_spin_warp(bar(Lay::bDS), par, wc, 1, 7))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        bwd::mma_ts_tile(tmem + kColDK, tmem + kColDP, desc_q_mn + s * kTileD, kIdTS, t > 0);
-        mma_commit(bar(Lay::bDK));
+        bwd::mma_ts_tile(tmem + col_acc, tmem + col_ss, desc_mn + s * kTileD, kIdTS, t > 0);
+        mma_commit(bar(b_acc));
         mma_commit(bar(Lay::bQE + s));
       }
       __syncwarp();
     }
-    if (!ok) {  // unwinding: wait for every MMA already issued
-      if (lane == 0) mma_commit(bar(Lay::bDR));
+    if (!ok) {  // unwinding: wait for every MMA this thread issued
+      const int dr = Lay::bDR + (chain_s ? 0 : 1);
+      if (lane == 0) mma_commit(bar(dr));
       __syncwarp();
-      mbar_wait_drain(bar(Lay::bDR), 0);
+      mbar_wait_drain(bar(dr), 0);
     }
   } else {
     // ================================================================ compute
@@ -366,6 +361,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // epilogue: the last dK commit covers every MMA of the CTA
     if (ok) ok = mbar_wait_warp(bar(Lay::bDK), static_cast<uint32_t>(n_it - 1) & 1u, wc, 2, 11);
+    if (ok) ok = mbar_wait_warp(bar(Lay::bDV), static_cast<uint32_t>(n_it - 1) & 1u, wc, 2, 11);
     if (ok) {
       tc_fence_after();
       const int key = j * kBN + r;
@@ -404,7 +400,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(Lay::bQ), 1);
     for (int s = 0; s < kBwdStagesQK; ++s) {
       mbar_init(bar(Lay::bKF + s), 1);
-      mbar_init(bar(Lay::bKE + s), 1);
+      mbar_init(bar(Lay::bKE + s), 2);  // read by S (warp 1) and dQ (warp 10)
     }
     for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(bar(Lay::bVF + s), 1);
@@ -418,6 +414,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(Lay::bDQ + b), 1);
     }
     mbar_init(bar(Lay::bDR), 1);
+    mbar_init(bar(Lay::bDR + 1), 1);
     fence_barrier_init();
     misc[1] = 0;
   }
@@ -524,8 +521,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           static_cast<uint32_t>(t / kBwdStages) & 1u);
       }
     }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
+  } else if (warp == 1 || warp == 10) {
+    // ================================ MMA issuers: S and dP on warp 1, dQ on warp 10
     constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
     const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);
@@ -533,63 +530,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);          // K-major use
     const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16, 1024);
     const uint64_t desc_k_mn = sdesc_sw128(sbase + Lay::kK, 16384, 1024);    // MN-major use
-    // S and dP of key tile jj + 1 are issued before dQ of tile jj waits for its dS, so the tensor
-    // pipe has them to execute while the compute warps form dS: dP alternates between two
-    // tensor-memory buffers, and a buffer is rewritten once the dQ product that read it (two
-    // tiles back) completed.
-    auto issue_s = [&](int jj) {
-      const int s = jj % kBwdStagesQK;
-      if (!mbar_wait_warp(bar(Lay::bKF + s), static_cast<uint32_t>(jj / kBwdStagesQK) & 1u, wc,
-                          1, 3))
-        return false;
-      // S rewrites the columns the compute threads read S_{jj-1} from
-      if (jj > 0 &&
-          !mbar_wait_spin_warp(bar(Lay::bSR), (static_cast<uint32_t>(jj) & 1u) ^ 1u, wc, 1, 4))
-        return false;
-      tc_fence_after();
-      if (lane == 0) {
-        bwd::mma_ss_tile<D>(tmem + kColS, desc_q, desc_k + s * kTileD, kIdSS);
-        mma_commit(bar(Lay::bS));
+    bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 2);
+    if (warp == 1) {
+      // S and dP run ahead of dQ: dP alternates between two tensor-memory buffers, and a buffer
+      // is rewritten once the dQ product that read it (two tiles back) completed; S is rewritten
+      // once every compute thread has read the previous one
+      for (int jj = 0; ok && jj < n_kv; ++jj) {
+        const int sk = jj % kBwdStagesQK, sv = jj % kBwdStages, b = jj & 1;
+        if (!(ok = mbar_wait_warp(bar(Lay::bKF + sk),
+                                  static_cast<uint32_t>(jj / kBwdStagesQK) & 1u, wc, 1, 3)))
+          break;
+        if (jj > 0 && !(ok = mbar_wait_spin_warp(bar(Lay::bSR), (static_cast<uint32_t>(jj) & 1u) ^ 1u,
+                                                 wc, 1, 4)))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+          bwd::mma_ss_tile<D>(tmem + kColS, desc_q, desc_k + sk * kTileD, kIdSS);
+          mma_commit(bar(Lay::bS));
+          mma_commit(bar(Lay::bKE + sk));
+        }
+        __syncwarp();
+        if (!(ok = mbar_wait_warp(bar(Lay::bVF + sv), static_cast<uint32_t>(jj / kBwdStages) & 1u,
+                                  wc, 1, 5)))
+          break;
+        if (jj >= 2 && !(ok = mbar_wait_spin_warp(bar(Lay::bDQ + b),
+                                                  (static_cast<uint32_t>(jj >> 1) & 1u) ^ 1u, wc,
+                                                  1, 6)))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+          bwd::mma_ss_tile<D>(tmem + kColDP[b], desc_do, desc_v + sv * kTileD, kIdSS);
+          mma_commit(bar(Lay::bDP + b));
+          mma_commit(bar(Lay::bVE + sv));
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      return true;
-    };
-    auto issue_dp = [&](int jj) {
-      const int s = jj % kBwdStages, b = jj & 1;
-      if (!mbar_wait_warp(bar(Lay::bVF + s), static_cast<uint32_t>(jj / kBwdStages) & 1u, wc, 1,
-                          5))
-        return false;
-      if (jj >= 2 &&  // the buffer's previous dS was read by dQ of tile jj - 2
-          !mbar_wait_spin_warp(bar(Lay::bDQ + b), (static_cast<uint32_t>(jj >> 1) & 1u) ^ 1u, wc, 1, 6))
-        return false;
-      tc_fence_after();
-      if (lane == 0) {
-        bwd::mma_ss_tile<D>(tmem + kColDP[b], desc_do, desc_v + s * kTileD, kIdSS);
-        mma_commit(bar(Lay::bDP + b));
-        mma_commit(bar(Lay::bVE + s));
+    } else {
+      for (int jj = 0; ok && jj < n_kv; ++jj) {
+        const int sk = jj % kBwdStagesQK, b = jj & 1;
+        if (!(ok = mbar_wait_spin_warp(bar(Lay::bDS + b), static_cast<uint32_t>(jj >> 1) & 1u, wc,
+                                       1, 7)))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+          bwd::mma_ts_tile(tmem + kColDQ, tmem + kColDP[b], desc_k_mn + sk * kTileD, kIdTS,
+                           jj > 0);
+          mma_commit(bar(Lay::bDQ + b));
+          mma_commit(bar(Lay::bKE + sk));
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      return true;
-    };
-    bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 2) && issue_s(0) && issue_dp(0);
-    for (int jj = 0; ok && jj < n_kv; ++jj) {
-      const int s = jj % kBwdStagesQK, b = jj & 1;
-      if (jj + 1 < n_kv && !(ok = issue_s(jj + 1) && issue_dp(jj + 1))) break;
-      if (!(ok = mbar_wait_spin_warp(bar(Lay::bDS + b), static_cast<uint32_t>(jj >> 1) & 1u, wc,
-                                     1, 7)))
-        break;
-      tc_fence_after();
-      if (lane == 0) {
-        bwd::mma_ts_tile(tmem + kColDQ, tmem + kColDP[b], desc_k_mn + s * kTileD, kIdTS, jj > 0);
-        mma_commit(bar(Lay::bDQ + b));
-        mma_commit(bar(Lay::bKE + s));
-      }
-      __syncwarp();
     }
-    if (!ok) {
-      if (lane == 0) mma_commit(bar(Lay::bDR));
+    if (!ok) {  // unwinding: wait for every MMA this thread issued
+      const int dr = Lay::bDR + (warp == 1 ? 0 : 1);
+      if (lane == 0) mma_commit(bar(dr));
       __syncwarp();
-      mbar_wait_drain(bar(Lay::bDR), 0);
+      mbar_wait_drain(bar(dr), 0);
     }
   } else {
     // ================================================================ compute
