@@ -9,7 +9,10 @@ synchronize on both sides.  Extra keys: ``e2e`` (the same metric through the pub
 pinned host buffers and every step's host<->device copies inside the timed region, steps
 pipelined over two device buffers; the serial loop beside it), ``roofline`` (the
 kernel against the measured bf16 tensor peak), ``cpu_baseline`` (the float64 oracle on a bounded
-sample), ``unfused`` (the three-kernel comparison path) and ``clocks``.
+sample), ``unfused`` (the three-kernel comparison path), ``configs`` (the fused forward on each
+of the five parity configurations: TFLOPS, achieved HBM GB/s on the algorithmic bytes and both
+roofline fractions), the grouped-query, split-KV, FP8, backward and packed-batch extras, and
+``clocks``.
 
 ``--impl reference`` times the float64 CPU oracle (the only reference this method has) on the
 host cores instead, on bounded samples of the same workload.
@@ -592,6 +595,49 @@ def run_ours(args, w, rank, world, dist):
                   "bwd_tflops": 2.5 * vf / (b_ms * 1e-3) / 1e12}
         del vq, vk, vv, vo, vl, vdo, vws
 
+    # ---- every named configuration (the five parity configurations) through the fused forward:
+    # time, TFLOPS (causal halved), achieved HBM bandwidth on the algorithmic bytes (read Q, K,
+    # V once, write O and LSE once) and both roofline fractions; the small-N cases are bound by
+    # latency and bandwidth, not by the tensor cores
+    per_config = None
+    if not args.no_extras:
+        per_config = []
+        hbm_peak = float(peaks["hbm_gbs"])
+        for idx in sorted(configs.WORKLOADS):
+            cw = configs.WORKLOADS[idx]
+            made = cw.make()
+            cq, ck, cv = to_dev(made[0]), to_dev(made[1]), to_dev(made[2])
+            cu_np = made[3] if cw.varlen else None
+            cu_d = torch.from_numpy(cu_np).to(dev) if cw.varlen else None
+            co, cl = attn.attn_fwd(cq, ck, cv, cu_seqlens=cu_d, causal=cw.causal, scale=cw.scale)
+
+            def call():
+                attn.attn_fwd(cq, ck, cv, cu_seqlens=cu_d, causal=cw.causal, scale=cw.scale,
+                              out=co, lse=cl)
+            for _ in range(3):
+                call()
+            barrier()
+            evs = []
+            for _ in range(20):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                evs.append((e0, e1))
+            barrier()
+            c_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+            lens = [int(x) for x in np.diff(cu_np)] if cw.varlen else [cw.N] * cw.B
+            c_flops = acc.attention_flops(cw.H, lens, cw.d, cw.causal)
+            c_bytes = acc.attention_ideal_bytes(cw.H, sum(lens), cw.d)
+            c_tf = c_flops / (c_ms * 1e-3) / 1e12
+            c_gbs = c_bytes / (c_ms * 1e-3) / 1e9
+            per_config.append({"workload": cw.name, "ms": c_ms, "tflops": c_tf,
+                               "tensor_frac": c_tf / peak, "algorithmic_bytes": c_bytes,
+                               "gbs": c_gbs, "hbm_frac": c_gbs / hbm_peak})
+            del cq, ck, cv, co, cl, cu_d
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
@@ -611,6 +657,7 @@ def run_ours(args, w, rank, world, dist):
             "pct_of_bf16_peak": 100.0 * value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "unfused": unfused,
             "gqa": gqa, "splitkv": splitkv, "backward": backward, "fp8": fp8, "varlen": varlen,
+            "configs": per_config,
             "clocks": clock_info, "gpu_launches": args.steps,
             "kernel_ms_median": statistics.median(per),
         }
