@@ -171,9 +171,11 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.part_stat = part_stat;
   p.n_qt = (N + 2 * kBM - 1) / (2 * kBM);  // pairs of 128-row query tiles per head
   p.scale_log2 = scale * 1.4426950408889634f;
+  // work units: (query pair, key slice) per head on the dense kernels, pair slots per head for
+  // packed batches; the two-tile kernel launches one CTA per unit, the two-SM kernel a
+  // persistent grid of clusters over the units
   const long long grid = varlen ? static_cast<long long>(p.n_qt + B) * H
-                                 : static_cast<long long>(p.n_qt) * B * H * n_splits *
-                                       (two_sm ? 2 : 1);
+                                 : static_cast<long long>(p.n_qt) * B * H * n_splits;
   if (grid > INT_MAX) return ATTN_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e =

@@ -7,30 +7,43 @@ namespace attn {
 namespace {
 
 template <bool CAUSAL>
-cudaError_t launch(const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch(const FwdParams& p, int units, cudaStream_t stream) {
   auto* kernel = attn_fwd_2sm_kernel<CAUSAL>;
   constexpr int kSmem = Fwd2smLayout::kDynBytes;
-  // the opt-in for more than 48 KB of dynamic shared memory is per device; remember it
-  static std::atomic<uint64_t> attr_done{0};
+  // the opt-in for more than 48 KB of dynamic shared memory and the number of clusters that fit
+  // at once are per device; remember them (0: not known yet)
+  static std::atomic<int> fit[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+  int clusters = fit[dev & 63].load(std::memory_order_acquire);
+  if (clusters == 0) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * kSmCount);
+    cfg.blockDim = dim3(k2smThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    int n = 0;
+    // the kernel's cluster shape (2, 1, 1) is a compile-time attribute
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = kSmCount / 2;
+    }
+    clusters = n;
+    fit[dev & 63].store(clusters, std::memory_order_release);
   }
-  // the kernel's cluster shape (2, 1, 1) is a compile-time attribute; grid is a multiple of 2
+  // persistent: one cluster of two CTAs per pair of SMs that fits, each looping over units
+  const int grid = 2 * (units < clusters ? units : clusters);
   kernel<<<grid, k2smThreads, kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, int grid, cudaStream_t stream) {
-  if (grid % 2 != 0) return cudaErrorInvalidValue;
-  return causal ? launch<true>(p, grid, stream) : launch<false>(p, grid, stream);
+cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, int units, cudaStream_t stream) {
+  if (units <= 0) return cudaErrorInvalidValue;
+  return causal ? launch<true>(p, units, stream) : launch<false>(p, units, stream);
 }
 
 }  // namespace attn

@@ -1,28 +1,35 @@
 // attn_fwd_2sm_kernel.cuh -- fused IO-aware attention forward for sm_103a (GB300), head dim 128,
 // one 128-row query tile per SM and one tensor-core product across the two SMs of a TPC.
 //
-// A cluster of two CTAs owns 256 consecutive query rows of one (sequence, head): the CTA of rank r
-// holds rows 128 r .. 128 r + 127 of them.  Each product is a single cta_group::2 MMA with M = 256
-// issued by rank 0: S = Q K_j^T takes A (Q) from each CTA's own rows and B (K_j) half from each
-// CTA (keys 64 r .. 64 r + 63 of the tile); O += P V_j takes P from each CTA's tensor memory and
-// V_j's value columns 64 r .. 64 r + 63 from CTA r.  So each SM streams half of every K and V tile
-// (the same K/V bytes per FLOP as two query tiles in one CTA) and holds one query tile, which
-// leaves tensor memory for three S buffers next to O: S_{j+3} can be issued as soon as
-// P_j V_j has completed, while the softmax works on S_{j+1} and S_{j+2}, so the softmax never
-// waits for a product that could have run earlier.  The tiled loop and online
-// softmax are those of the FlashAttention forward (CS336 Lecture 5 notes, section 6.2; the block
-// merge of the CS336 GPU/attention notes, "Online softmax 回顾").
+// A cluster of two CTAs works on 256 consecutive query rows of one (sequence, head) at a time:
+// the CTA of rank r holds rows 128 r .. 128 r + 127 of them.  Each product is a single
+// cta_group::2 MMA with M = 256 issued by rank 0: S = Q K_j^T takes A (Q) from each CTA's own rows
+// and B (K_j) half from each CTA (keys 64 r .. 64 r + 63 of the tile); O += P V_j takes P from
+// each CTA's tensor memory and V_j's value columns 64 r .. 64 r + 63 from CTA r.  So each SM
+// streams half of every K and V tile (the same K/V bytes per FLOP as two query tiles in one CTA)
+// and holds one query tile, which leaves tensor memory for three S buffers next to O: S_{j+3} can
+// be issued as soon as P_j V_j has completed, while the softmax works on S_{j+1} and S_{j+2}.
+// The tiled loop and online softmax are those of the FlashAttention forward (CS336 Lecture 5
+// notes, section 6.2; the block merge of the CS336 GPU/attention notes, "Online softmax 回顾").
+//
+// The kernel is persistent: the grid holds as many clusters as fit on the GPU at once, and
+// cluster c takes the work units (query pair, key slice) c, 2G - 1 - c, 2G + c, 4G - 1 - c, ...
+// of the non-persistent grid's order (causal: heaviest first), a mix of heavy and light ones.
+// Q is double-buffered, and the K/V rings, the S buffers and every barrier phase run on across
+// units, so the next unit's Q load and first S products overlap the current unit's last tiles
+// and epilogue; only its first P V waits, for the epilogue to have read O.
 //
 // Warp roles (224 threads per CTA):
-//   warp 0      TMA producer of this CTA's halves: Q once, K_j and V_j into four-stage rings.
-//               Completion is counted on rank 0's barriers.
+//   warp 0      TMA producer of this CTA's halves: Q per unit, K_j and V_j into four-stage
+//               rings.  Completion is counted on rank 0's barriers.
 //   warp 1      tensor memory allocation (both CTAs); on rank 0 lane 0 issues the P V products.
-//   warps 2..5  softmax: one query row per thread (the TMEM lane its warp may access).
+//   warps 2..5  softmax: one query row per thread (the TMEM lane its warp may access), and the
+//               epilogue of each unit.
 //   warp 6      on rank 0 lane 0 issues the S products, up to three key tiles ahead.
 //
-// Tensor memory (512 columns in each SM): S buffers at 0, 128, 256 (fp32 128 x 128, key tile j in
-// buffer j % 3), O at 384.  P_j (bf16, two per column) overwrites the first 64 columns of its S
-// buffer once the softmax has read it.
+// Tensor memory (512 columns in each SM): S buffers at 0, 128, 256 (fp32 128 x 128; the g-th key
+// tile the cluster processes, counted across units, uses buffer g % 3), O at 384.  P (bf16, two
+// per column) overwrites the first 64 columns of its S buffer once the softmax has read it.
 //
 // Softmax in the exp2 domain, with the same sum-triggered reference maximum as the two-tile
 // kernel: a tile is exponentiated against the row's reference m first, and its maximum is taken
@@ -51,6 +58,44 @@ __device__ __forceinline__ void settle(unsigned long long ns) {
   const unsigned long long t0 = global_timer_ns();
   while (global_timer_ns() - t0 < ns) {
   }
+}
+
+// One work unit: 256 query rows of a head and a slice of their key tiles.
+struct Unit {
+  int z;      // head slice of the tensor maps
+  int pt;     // query pair within the sequence
+  int split;  // key slice
+  int kb;     // first key tile of the slice
+  int n;      // key tiles of the slice (0: nothing to do)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit unit_of(const FwdParams& p, int u) {
+  Unit w;
+  const int BH = p.B * p.H;
+  const int L = u / p.n_splits;
+  w.split = u % p.n_splits;
+  if constexpr (CAUSAL) {  // heaviest pairs (most key tiles) first
+    w.pt = p.n_qt - 1 - L / BH;
+    w.z = L % BH;
+  } else {                 // all pairs of a head together: its K and V stay in L2
+    w.z = L / p.n_qt;
+    w.pt = L % p.n_qt;
+  }
+  // key tiles of the row pair (causal: up to the diagonal of its last row); both CTAs run the
+  // same count, rank 0's rows of a tile past their diagonal are fully masked
+  const int n_keytiles = (p.N + kBN - 1) / kBN;
+  const int n_full = CAUSAL ? min(n_keytiles, 2 * w.pt + 2) : n_keytiles;
+  const int chunk = (n_full + p.n_splits - 1) / p.n_splits;
+  w.kb = w.split * chunk;
+  w.n = max(0, min(w.kb + chunk, n_full) - w.kb);
+  return w;
+}
+
+// The k-th unit of cluster c among G clusters: rounds of G units, taken forward in even rounds
+// and backward in odd ones, so that with units ordered heaviest first every cluster gets a mix.
+__device__ __forceinline__ int next_unit(int k, int c, int G) {
+  return k * G + ((k & 1) ? G - 1 - c : c);
 }
 
 }  // namespace fwd2sm
@@ -83,49 +128,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- the 256 query rows of this cluster: z = head slice of the tensor maps, pt = row pair;
-  // with split-KV, consecutive clusters are the key slices of one row pair
-  const int BH = p.B * p.H;
-  const int L = (static_cast<int>(blockIdx.x) >> 1) / p.n_splits;
-  const int split = (static_cast<int>(blockIdx.x) >> 1) % p.n_splits;
-  int z, pt;
-  if constexpr (CAUSAL) {  // heaviest pairs (most key tiles) first
-    pt = p.n_qt - 1 - L / BH;
-    z = L % BH;
-  } else {                 // all pairs of a head together: its K and V stay in L2
-    z = L / p.n_qt;
-    pt = L % p.n_qt;
-  }
+  const int n_units = p.n_qt * p.B * p.H * p.n_splits;
+  const int G = static_cast<int>(gridDim.x) >> 1;  // clusters in the grid
+  const int c0 = static_cast<int>(blockIdx.x) >> 1;
   const int seq_len = p.N;
-  const int n_keytiles = (seq_len + kBN - 1) / kBN;
-  // key tiles of the row pair (causal: up to the diagonal of its last row); both CTAs run the
-  // same count, rank 0's rows of a tile past their diagonal are fully masked.  This cluster takes
-  // key tiles [kb, kb + n) of them; pipeline bookkeeping runs over j = 0..n-1, key tile kb + j is
-  // the data.
-  const int n_full = CAUSAL ? min(n_keytiles, 2 * pt + 2) : n_keytiles;
-  const int chunk = (n_full + p.n_splits - 1) / p.n_splits;
-  const int kb = split * chunk;
-  const int n = max(0, min(kb + chunk, n_full) - kb);
-  const int qrow0 = (2 * pt + static_cast<int>(rank)) * kBM;  // first row of this CTA's tile
-  const int z_kv = (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
-  if (n == 0) {
-    // a key slice past the end of this pair's range (uniform for the cluster, before any
-    // cluster-wide step): the merge reads max -inf and sum 0 for these rows
-    const size_t rows_total = static_cast<size_t>(p.B) * p.H * p.N;
-    const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
-    const int row = qrow0 + static_cast<int>(threadIdx.x);
-    if (threadIdx.x < kBM && row < seq_len) {
-      const size_t slot = static_cast<size_t>(split) * rows_total +
-                          static_cast<size_t>(z) * static_cast<size_t>(p.N) + row;
-      p.part_stat[slot] = -INFINITY;
-      p.part_stat[plane + slot] = 0.f;
-    }
-    return;
-  }
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(Lay::bQ), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(Lay::bQF + b), 1);
+      mbar_init(bar(Lay::bQE + b), 1);
+    }
     for (int s = 0; s < SK; ++s) {
       mbar_init(bar(Lay::bKF + s), 1);
       mbar_init(bar(Lay::bKE + s), 1);
@@ -140,6 +152,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       mbar_init(bar(Lay::bPV + b), 1);
     }
     mbar_init(bar(Lay::bOD), 1);
+    mbar_init(bar(Lay::bOE), 2 * 4);
     mbar_init(bar(Lay::bDR), 1);
     mbar_init(bar(Lay::bDR + 1), 1);
     fence_barrier_init();
@@ -154,6 +167,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
+  // Counters kept by every role: uq = units with work done so far (selects the Q buffer and the
+  // per-unit barrier phases), g = key tiles done so far across units (ring stages, S buffers and
+  // their phases).
   if (warp == 0) {
     // ===================================================================== TMA producer
     if (lane == 0) {
@@ -162,83 +178,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       tma_prefetch_desc(&p.tm_v);
       const uint64_t keep = l2_policy_evict_last();   // K/V are re-read by every query pair
       const uint64_t once = l2_policy_evict_first();  // Q is read once
-      if (leader) mbar_arrive_expect_tx(bar(Lay::bQ), 2 * Lay::kQBytes);
-      #pragma unroll
-      for (int c = 0; c < 2; ++c)
-        tma_load_3d_pair(sbase + Lay::kQ + c * 16384, &p.tm_q, lbar(Lay::bQ), c * 64, qrow0, z,
-                         once);
-      int nk = 0, nv = 0;
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int sk = j % SK, sv = j % SV;
-        if (j >= SK &&
-            !(ok = mbar_wait(bar(Lay::bKE + sk), (static_cast<uint32_t>(j / SK) & 1u) ^ 1u, wc,
-                             0, 1)))
+      int g = 0, uq = 0;
+      for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
+        const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
+        if (w.n == 0) continue;
+        const int qb = uq & 1;
+        const int z_kv = (w.z / p.H) * (p.H / p.group) + (w.z % p.H) / p.group;
+        // the Q buffer was last used by unit uq - 2: its S products have completed
+        if (uq >= 2 && !(ok = mbar_wait(bar(Lay::bQE + qb),
+                                        static_cast<uint32_t>((uq - 2) >> 1) & 1u, wc, 0, 3)))
           break;
-        if (leader) mbar_arrive_expect_tx(bar(Lay::bKF + sk), 2 * Lay::kKBytes);
+        if (leader) mbar_arrive_expect_tx(bar(Lay::bQF + qb), 2 * Lay::kQBytes);
+        const int qrow0 = (2 * w.pt + static_cast<int>(rank)) * kBM;
         #pragma unroll
         for (int c = 0; c < 2; ++c)
-          tma_load_3d_pair(sbase + Lay::kK + sk * Lay::kKBytes + c * 8192, &p.tm_k,
-                           lbar(Lay::bKF + sk), c * 64,
-                           (kb + j) * kBN + 64 * static_cast<int>(rank), z_kv, keep);
-        ++nk;
-        if (j >= SV &&
-            !(ok = mbar_wait(bar(Lay::bVE + sv), (static_cast<uint32_t>(j / SV) & 1u) ^ 1u, wc,
-                             0, 2)))
-          break;
-        if (leader) mbar_arrive_expect_tx(bar(Lay::bVF + sv), 2 * Lay::kVBytes);
-        tma_load_3d_pair(sbase + Lay::kV + sv * Lay::kVBytes, &p.tm_v, lbar(Lay::bVF + sv),
-                         64 * static_cast<int>(rank), (kb + j) * kBN, z_kv, keep);
-        ++nv;
-      }
-      if (!ok) {  // unwinding: let every copy still in flight land before the cluster exits
-        if (leader) {
-          mbar_wait_drain(bar(Lay::bQ), 0);
-          for (int j = (nk > SK ? nk - SK : 0); j < nk; ++j)
-            mbar_wait_drain(bar(Lay::bKF + j % SK), static_cast<uint32_t>(j / SK) & 1u);
-          for (int j = (nv > SV ? nv - SV : 0); j < nv; ++j)
-            mbar_wait_drain(bar(Lay::bVF + j % SV), static_cast<uint32_t>(j / SV) & 1u);
-        } else {
-          fwd2sm::settle(100000ull);  // completion is counted on rank 0's barriers
+          tma_load_3d_pair(sbase + Lay::kQ + qb * Lay::kQBytes + c * 16384, &p.tm_q,
+                           lbar(Lay::bQF + qb), c * 64, qrow0, w.z, once);
+        for (int j = 0; j < w.n; ++j, ++g) {
+          const int sk = g % SK, sv = g % SV;
+          if (g >= SK &&
+              !(ok = mbar_wait(bar(Lay::bKE + sk), (static_cast<uint32_t>(g / SK) & 1u) ^ 1u, wc,
+                               0, 1)))
+            break;
+          if (leader) mbar_arrive_expect_tx(bar(Lay::bKF + sk), 2 * Lay::kKBytes);
+          #pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d_pair(sbase + Lay::kK + sk * Lay::kKBytes + c * 8192, &p.tm_k,
+                             lbar(Lay::bKF + sk), c * 64,
+                             (w.kb + j) * kBN + 64 * static_cast<int>(rank), z_kv, keep);
+          if (g >= SV &&
+              !(ok = mbar_wait(bar(Lay::bVE + sv), (static_cast<uint32_t>(g / SV) & 1u) ^ 1u, wc,
+                               0, 2)))
+            break;
+          if (leader) mbar_arrive_expect_tx(bar(Lay::bVF + sv), 2 * Lay::kVBytes);
+          tma_load_3d_pair(sbase + Lay::kV + sv * Lay::kVBytes, &p.tm_v, lbar(Lay::bVF + sv),
+                           64 * static_cast<int>(rank), (w.kb + j) * kBN, z_kv, keep);
         }
+        ++uq;
       }
+      // unwinding: copies in flight signal rank 0's barriers and land within microseconds;
+      // let them land before the cluster exits
+      if (!ok) fwd2sm::settle(100000ull);
     }
   } else if (warp == 1 || warp == kSIssuerWarp) {
     // ========================================= MMA issuers (rank 0): P V on warp 1, S on warp 6
     // Two issuing threads, so that each one's waits overlap the other's products: an MMA issue
     // blocks until the tensor pipe accepts it, so one thread issuing both products leaves the
-    // pipe idle during every wait.  S_j needs only K_j and the completion of P_{j-3} V_{j-3}
-    // (its buffer held P_{j-3}); P_j V_j needs P_j and V_j.
+    // pipe idle during every wait.  S_g needs K_g and the completion of P_{g-3} V_{g-3} (its
+    // buffer held P_{g-3}); P_g V_g needs P_g and V_g, and the first P V of a unit also needs the
+    // previous unit's epilogue to have read O.
     if (leader) {
-      bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 4);
+      bool ok = true;
+      int g = 0, uq = 0;
       if (warp == kSIssuerWarp) {
         constexpr uint32_t kIdS = idesc_bf16_f32(2 * kBM, kBN, false, false);  // Q, K K-major
-        const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);
         const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
-        for (int j = 0; ok && j < n; ++j) {
-          // the S issuer runs ahead of the softmax: its waits may suspend (spinning here took
-          // issue slots from the softmax warp on the same sub-partition)
-          if (j >= NB && !(ok = mbar_wait_warp(bar(Lay::bPV + j % NB),
-                                               static_cast<uint32_t>((j - NB) / NB) & 1u, wc, 1,
-                                               7)))
+        for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
+          const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
+          if (w.n == 0) continue;
+          const int qb = uq & 1;
+          const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ + qb * Lay::kQBytes, 16, 1024);
+          if (!(ok = mbar_wait_warp(bar(Lay::bQF + qb), static_cast<uint32_t>(uq >> 1) & 1u, wc,
+                                    1, 4)))
             break;
-          if (!(ok = mbar_wait_warp(bar(Lay::bKF + j % SK), static_cast<uint32_t>(j / SK) & 1u,
-                                    wc, 1, 3)))
-            break;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint64_t b = desc_k + static_cast<uint64_t>((j % SK) * (Lay::kKBytes >> 4));
-            const uint32_t d = tmem + 128u * static_cast<uint32_t>(j % NB);
-            #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {  // K = 16 per instruction; 4 steps per 128 bytes
-              const uint64_t oq = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
-              const uint64_t ok_ = static_cast<uint64_t>(((k >> 2) * 8192 + (k & 3) * 32) >> 4);
-              mma_bf16_ss_pair(d, desc_q + oq, b + ok_, kIdS, k > 0 ? 1u : 0u);
+          for (int j = 0; j < w.n; ++j, ++g) {
+            // the S issuer runs ahead of the softmax: its waits may suspend (spinning here took
+            // issue slots from the softmax warp on the same sub-partition)
+            if (g >= NB && !(ok = mbar_wait_warp(bar(Lay::bPV + g % NB),
+                                                 static_cast<uint32_t>((g - NB) / NB) & 1u, wc, 1,
+                                                 7)))
+              break;
+            if (!(ok = mbar_wait_warp(bar(Lay::bKF + g % SK), static_cast<uint32_t>(g / SK) & 1u,
+                                      wc, 1, 3)))
+              break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t b = desc_k + static_cast<uint64_t>((g % SK) * (Lay::kKBytes >> 4));
+              const uint32_t d = tmem + 128u * static_cast<uint32_t>(g % NB);
+              #pragma unroll
+              for (int k = 0; k < D / 16; ++k) {  // K = 16 per instruction; 4 per 128 bytes
+                const uint64_t oq = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+                const uint64_t ok_ = static_cast<uint64_t>(((k >> 2) * 8192 + (k & 3) * 32) >> 4);
+                mma_bf16_ss_pair(d, desc_q + oq, b + ok_, kIdS, k > 0 ? 1u : 0u);
+              }
+              mma_commit_pair(bar(Lay::bSF + g % NB), kBoth);
+              mma_commit_pair(bar(Lay::bKE + g % SK), kBoth);
+              if (j == w.n - 1) mma_commit_pair(bar(Lay::bQE + qb), kBoth);
             }
-            mma_commit_pair(bar(Lay::bSF + j % NB), kBoth);
-            mma_commit_pair(bar(Lay::bKE + j % SK), kBoth);
+            __syncwarp();
           }
-          __syncwarp();
+          ++uq;
         }
         if (!ok) {  // unwinding: wait for every MMA this thread issued
           if (lane == 0) mma_commit_pair(bar(Lay::bDR), 0x1);
@@ -248,28 +278,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       } else {
         constexpr uint32_t kIdO = idesc_bf16_f32(2 * kBM, D, false, true);  // P (TMEM), V MN
         const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16384, 1024);
-        for (int j = 0; ok && j < n; ++j) {
-          const int b = j % NB, sv = j % SV;
-          if (!(ok = mbar_wait_spin_lane0(bar(Lay::bVF + sv), static_cast<uint32_t>(j / SV) & 1u,
-                                          wc, 1, 6)))
-            break;
-          if (!(ok = mbar_wait_spin_lane0(bar(Lay::bPF + b), static_cast<uint32_t>(j / NB) & 1u,
-                                          wc, 1, 5)))
-            break;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint64_t bv = desc_v + static_cast<uint64_t>(sv * (Lay::kVBytes >> 4));
-            const uint32_t a = tmem + 128u * static_cast<uint32_t>(b);
-            #pragma unroll
-            for (int k = 0; k < kBN / 16; ++k)  // 16 keys (2048 bytes of V) per instruction
-              mma_bf16_ts_pair(tmem + kColO, a + k * 8,
-                               bv + static_cast<uint64_t>(k * (2048 >> 4)), kIdO,
-                               (j > 0 || k > 0) ? 1u : 0u);
-            mma_commit_pair(bar(Lay::bPV + b), kBoth);
-            mma_commit_pair(bar(Lay::bVE + sv), kBoth);
-            if (j == n - 1) mma_commit_pair(bar(Lay::bOD), kBoth);
+        for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
+          const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
+          if (w.n == 0) continue;
+          for (int j = 0; j < w.n; ++j, ++g) {
+            const int b = g % NB, sv = g % SV;
+            if (!(ok = mbar_wait_spin_lane0(bar(Lay::bVF + sv),
+                                            static_cast<uint32_t>(g / SV) & 1u, wc, 1, 6)))
+              break;
+            if (!(ok = mbar_wait_spin_lane0(bar(Lay::bPF + b), static_cast<uint32_t>(g / NB) & 1u,
+                                            wc, 1, 5)))
+              break;
+            // the first product of a unit overwrites O: the previous unit's epilogue read it
+            if (j == 0 && uq > 0 &&
+                !(ok = mbar_wait_spin_lane0(bar(Lay::bOE), static_cast<uint32_t>(uq - 1) & 1u, wc,
+                                            1, 8)))
+              break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t bv = desc_v + static_cast<uint64_t>(sv * (Lay::kVBytes >> 4));
+              const uint32_t a = tmem + 128u * static_cast<uint32_t>(b);
+              #pragma unroll
+              for (int k = 0; k < kBN / 16; ++k)  // 16 keys (2048 bytes of V) per instruction
+                mma_bf16_ts_pair(tmem + kColO, a + k * 8,
+                                 bv + static_cast<uint64_t>(k * (2048 >> 4)), kIdO,
+                                 (j > 0 || k > 0) ? 1u : 0u);
+              mma_commit_pair(bar(Lay::bPV + b), kBoth);
+              mma_commit_pair(bar(Lay::bVE + sv), kBoth);
+              if (j == w.n - 1) mma_commit_pair(bar(Lay::bOD), kBoth);
+            }
+            __syncwarp();
           }
-          __syncwarp();
+          if (!ok) break;
+          ++uq;
         }
         if (!ok) {
           if (lane == 0) mma_commit_pair(bar(Lay::bDR + 1), 0x1);
@@ -282,172 +323,190 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
     // ===================================================================== softmax
     const int quarter = warp & 3;       // TMEM lanes this warp may access: 32*quarter .. +31
     const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
-    const int row = qrow0 + r;          // row within the sequence
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t o_col = t_lane + kColO;
     const float sl2 = p.scale_log2;
-    float m2 = -INFINITY;                // reference max of the scaled scores (log2 units)
-    float le[4] = {0.f, 0.f, 0.f, 0.f};  // sums of 2^(t - m), fp32
+    const size_t rows_total = static_cast<size_t>(p.B) * p.H * p.N;
+    const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int b = j % NB;
-      if (!(ok = mbar_wait_warp(bar(Lay::bSF + b), static_cast<uint32_t>(j / NB) & 1u, wc, 2,
-                                8)))
-        break;
-      tc_fence_after();
-      const uint32_t s_col = t_lane + 128u * static_cast<uint32_t>(b);
-      uint32_t u0[32], u1[32], u2[32], u3[32];
-      tmem_ld32(s_col + 0, u0);
-      tmem_ld32(s_col + 32, u1);
-      tmem_ld32(s_col + 64, u2);
-      tmem_ld32(s_col + 96, u3);
-      tmem_wait_ld_regs(u0);
-      tmem_wait_ld_regs(u1);
-      tmem_wait_ld_regs(u2);
-      tmem_wait_ld_regs(u3);
-      float s[128];
-      #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        s[i] = u2f(u0[i]);
-        s[32 + i] = u2f(u1[i]);
-        s[64 + i] = u2f(u2[i]);
-        s[96 + i] = u2f(u3[i]);
-      }
-      const int key0 = (kb + j) * kBN;
-      if ((CAUSAL && key0 + kBN - 1 > qrow0) || key0 + kBN > seq_len) {
-        const int lim = CAUSAL ? min(seq_len - key0, row - key0 + 1) : (seq_len - key0);
-        #pragma unroll
-        for (int c = 0; c < kBN; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
-      }
-      // P = 2^(t - m) in bf16, two per 32-bit word, over the first 64 columns of the buffer;
-      // ts = this tile's row sums.  Pass 0 exponentiates against the current reference; the row
-      // maximum is taken (pass 1) only on the first tile or when a row's tile sum exceeds
-      // kSumLimit.  Both passes are warp-uniform: the TMEM stores are collective.
-      float ts[4];
-      bool moved = false;
-      float alpha = 1.f;
-      bool need = (j == 0);
-      #pragma unroll 1
-      for (int pass = (j == 0) ? 1 : 0; pass < 2; ++pass) {
-        float m_use = m2;
-        if (pass == 1) {
-          float mx[8];
-          #pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = s[k];
-          #pragma unroll
-          for (int c = 8; c < kBN; c += 16)
-            #pragma unroll
-            for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[c + k], s[c + 8 + k]);
-          const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmaxf(mx[6], mx[7])) * sl2;
-          const float m_new = need ? fmaxf(mt, m2) : m2;
-          moved = (m_new != m2);
-          m_use = (m_new == -INFINITY) ? 0.f : m_new;
-          alpha = moved ? ex2_approx(m2 - m_use) : 1.f;
-          m2 = m_new;
-          if (moved) {
-            #pragma unroll
-            for (int k = 0; k < 4; ++k) le[k] *= alpha;
-          }
-          tmem_wait_st();  // pass 0's stores land before these overwrite them
+    int g = 0, uq = 0;
+    for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
+      const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
+      const int qrow0 = (2 * w.pt + static_cast<int>(rank)) * kBM;  // first row of this tile
+      const int row = qrow0 + r;                                     // row within the sequence
+      const bool valid = row < seq_len;
+      const size_t grow = static_cast<size_t>(w.z) * static_cast<size_t>(p.N) +
+                          static_cast<size_t>(row);
+      if (w.n == 0) {
+        // a key slice past the end of this pair's range: the merge reads max -inf and sum 0
+        if (valid) {
+          const size_t slot = static_cast<size_t>(w.split) * rows_total + grow;
+          p.part_stat[slot] = -INFINITY;
+          p.part_stat[plane + slot] = 0.f;
         }
-        const float neg_m = -m_use;
-        #pragma unroll
-        for (int k = 0; k < 4; ++k) ts[k] = 0.f;
-        #pragma unroll
-        for (int h = 0; h < 4; ++h) {  // quarters of 32 keys: 16 packed words each
-          uint32_t pk[16];
-          #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = 32 * h + 2 * i;
-            float x0, x1;
-            ffma2(x0, x1, s[c], s[c + 1], sl2, sl2, neg_m, neg_m);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            pk[i] = pack_bf16x2(p0, p1);
-            fadd2(ts[2 * (i & 1)], ts[2 * (i & 1) + 1], p0, p1);
-          }
-          tmem_st16(s_col + 16 * h, pk);
-        }
-        if (pass == 0) {
-          need = !(((ts[0] + ts[1]) + (ts[2] + ts[3])) <= kSumLimit);  // also catches inf, NaN
-          if (!__any_sync(0xffffffffu, need)) break;
-        }
+        continue;
       }
-      #pragma unroll
-      for (int k = 0; k < 4; ++k) le[k] += ts[k];
-
-      // O holds P V up to key tile j-1 once that product completes; bring it to the new
-      // reference before P_j V_j is added
-      if (j > 0 && __any_sync(0xffffffffu, moved)) {
-        if (!(ok = mbar_wait_warp(bar(Lay::bPV + (j - 1) % NB),
-                                  static_cast<uint32_t>((j - 1) / NB) & 1u, wc, 2, 9)))
+      float m2 = -INFINITY;                // reference max of the scaled scores (log2 units)
+      float le[4] = {0.f, 0.f, 0.f, 0.f};  // sums of 2^(t - m), fp32
+      for (int j = 0; j < w.n; ++j, ++g) {
+        const int b = g % NB;
+        if (!(ok = mbar_wait_warp(bar(Lay::bSF + b), static_cast<uint32_t>(g / NB) & 1u, wc, 2,
+                                  8)))
           break;
         tc_fence_after();
+        const uint32_t s_col = t_lane + 128u * static_cast<uint32_t>(b);
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(s_col + 0, u0);
+        tmem_ld32(s_col + 32, u1);
+        tmem_ld32(s_col + 64, u2);
+        tmem_ld32(s_col + 96, u3);
+        tmem_wait_ld_regs(u0);
+        tmem_wait_ld_regs(u1);
+        tmem_wait_ld_regs(u2);
+        tmem_wait_ld_regs(u3);
+        float s[128];
         #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_col + c * 32, o);
-          tmem_wait_ld_regs(o);
-          #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-          tmem_st32(o_col + c * 32, o);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = u2f(u0[i]);
+          s[32 + i] = u2f(u1[i]);
+          s[64 + i] = u2f(u2[i]);
+          s[96 + i] = u2f(u3[i]);
         }
+        const int key0 = (w.kb + j) * kBN;
+        if ((CAUSAL && key0 + kBN - 1 > qrow0) || key0 + kBN > seq_len) {
+          const int lim = CAUSAL ? min(seq_len - key0, row - key0 + 1) : (seq_len - key0);
+          #pragma unroll
+          for (int cc = 0; cc < kBN; ++cc) s[cc] = (cc < lim) ? s[cc] : -INFINITY;
+        }
+        // P = 2^(t - m) in bf16, two per 32-bit word, over the first 64 columns of the buffer;
+        // ts = this tile's row sums.  Pass 0 exponentiates against the current reference; the
+        // row maximum is taken (pass 1) only on the first tile or when a row's tile sum exceeds
+        // kSumLimit.  Both passes are warp-uniform: the TMEM stores are collective.
+        float ts[4];
+        bool moved = false;
+        float alpha = 1.f;
+        bool need = (j == 0);
+        #pragma unroll 1
+        for (int pass = (j == 0) ? 1 : 0; pass < 2; ++pass) {
+          float m_use = m2;
+          if (pass == 1) {
+            float mx[8];
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = s[k];
+            #pragma unroll
+            for (int cc = 8; cc < kBN; cc += 16)
+              #pragma unroll
+              for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[cc + k], s[cc + 8 + k]);
+            const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                   fmaxf(mx[6], mx[7])) * sl2;
+            const float m_new = need ? fmaxf(mt, m2) : m2;
+            moved = (m_new != m2);
+            m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            alpha = moved ? ex2_approx(m2 - m_use) : 1.f;
+            m2 = m_new;
+            if (moved) {
+              #pragma unroll
+              for (int k = 0; k < 4; ++k) le[k] *= alpha;
+            }
+            tmem_wait_st();  // pass 0's stores land before these overwrite them
+          }
+          const float neg_m = -m_use;
+          #pragma unroll
+          for (int k = 0; k < 4; ++k) ts[k] = 0.f;
+          #pragma unroll
+          for (int h = 0; h < 4; ++h) {  // quarters of 32 keys: 16 packed words each
+            uint32_t pk[16];
+            #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int cc = 32 * h + 2 * i;
+              float x0, x1;
+              ffma2(x0, x1, s[cc], s[cc + 1], sl2, sl2, neg_m, neg_m);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              pk[i] = pack_bf16x2(p0, p1);
+              fadd2(ts[2 * (i & 1)], ts[2 * (i & 1) + 1], p0, p1);
+            }
+            tmem_st16(s_col + 16 * h, pk);
+          }
+          if (pass == 0) {
+            need = !(((ts[0] + ts[1]) + (ts[2] + ts[3])) <= kSumLimit);  // also catches inf, NaN
+            if (!__any_sync(0xffffffffu, need)) break;
+          }
+        }
+        #pragma unroll
+        for (int k = 0; k < 4; ++k) le[k] += ts[k];
+
+        // O holds P V up to key tile j-1 once that product completes; bring it to the new
+        // reference before P_j V_j is added
+        if (j > 0 && __any_sync(0xffffffffu, moved)) {
+          if (!(ok = mbar_wait_warp(bar(Lay::bPV + (g - 1) % NB),
+                                    static_cast<uint32_t>((g - 1) / NB) & 1u, wc, 2, 9)))
+            break;
+          tc_fence_after();
+          #pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(o_col + cc * 32, o);
+            tmem_wait_ld_regs(o);
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+            tmem_st32(o_col + cc * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lbar(Lay::bPF + b));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(lbar(Lay::bPF + b));
-    }
-    if (ok) ok = mbar_wait_warp(bar(Lay::bOD), 0, wc, 2, 10);
-    const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
-    const bool valid = row < seq_len;
-    const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
-                        static_cast<size_t>(row);
-    if (p.n_splits > 1) {
-      // this key slice's partial result for the merge: unnormalised O, reference max and row sum
-      const size_t rows_total = static_cast<size_t>(p.B) * p.H * p.N;
-      const size_t slot = static_cast<size_t>(split) * rows_total + grow;
-      const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
-      if (valid) {
-        p.part_stat[slot] = ok ? m2 : -INFINITY;
-        p.part_stat[plane + slot] = ok ? l_exact : 0.f;
-      }
-      if (ok) {
-        tc_fence_after();
+      if (!ok) break;
+      // ---- epilogue of the unit: O (and the row statistics) out, then O is free again
+      if (!(ok = mbar_wait_warp(bar(Lay::bOD), static_cast<uint32_t>(uq) & 1u, wc, 2, 10))) break;
+      tc_fence_after();
+      const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
+      if (p.n_splits > 1) {
+        // this key slice's partial result for the merge: unnormalised O, reference max, row sum
+        const size_t slot = static_cast<size_t>(w.split) * rows_total + grow;
+        if (valid) {
+          p.part_stat[slot] = m2;
+          p.part_stat[plane + slot] = l_exact;
+        }
         float4* prow = reinterpret_cast<float4*>(p.part_o + slot * D);
         #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(o_col + c * 32, o);
+          tmem_ld32(o_col + cc * 32, o);
           tmem_wait_ld_regs(o);
           if (valid) {
             #pragma unroll
             for (int q = 0; q < 8; ++q)
-              prow[c * 8 + q] = make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]),
-                                            u2f(o[4 * q + 3]));
+              prow[cc * 8 + q] = make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]),
+                                             u2f(o[4 * q + 3]));
           }
         }
-      }
-    } else if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.f / l_exact;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);
-      #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(o_col + c * 32, o);
-        tmem_wait_ld_regs(o);
-        uint32_t pk[16];
+      } else {
+        const float inv_l = 1.f / l_exact;
+        uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);
         #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
-        if (valid) {
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_col + cc * 32, o);
+          tmem_wait_ld_regs(o);
+          uint32_t pk[16];
           #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            orow[c * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+          if (valid) {
+            #pragma unroll
+            for (int q = 0; q < 4; ++q)
+              orow[cc * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
         }
+        if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
       }
-      if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
+      // every load of O has completed (wait::ld above); the next unit's first P V may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lbar(Lay::bOE));
+      ++uq;
     }
   }
   tc_fence_before();

@@ -76,21 +76,23 @@ struct Fwd2smLayout {
   static constexpr int kQBytes = kBM * 128 * 2;  // this CTA's 128 query rows (two 64-col blocks)
   static constexpr int kKBytes = 64 * 128 * 2;   // 64 keys of a key tile (two 8 KB blocks)
   static constexpr int kVBytes = kBN * 64 * 2;   // a key tile's 64 value columns of this CTA
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kQ = 0;                   // [2]: the current and the next query pair
+  static constexpr int kK = kQ + 2 * kQBytes;
   static constexpr int kV = kK + k2smStagesK * kKBytes;
   static constexpr int kBar = kV + k2smStagesV * kVBytes;
   enum {
-    bQ = 0,                        // both CTAs' Q landed (leader's copy)
-    bKF = 1,                       // K stage full (leader's copy)  [k2smStagesK]
+    bQF = 0,                       // both CTAs' Q landed (leader's copy)   [2 Q buffers]
+    bQE = bQF + 2,                 // Q buffer free: its S products done (both) [2]
+    bKF = bQE + 2,                 // K stage full (leader's copy)  [k2smStagesK]
     bKE = bKF + k2smStagesK,       // K stage free (both)           [k2smStagesK]
     bVF = bKE + k2smStagesK,       // V stage full (leader's copy)  [k2smStagesV]
     bVE = bVF + k2smStagesV,       // V stage free (both)           [k2smStagesV]
     bSF = bVE + k2smStagesV,       // S written into buffer b (both)          [k2smSBufs]
     bPF = bSF + k2smSBufs,         // P written, O corrected (leader's copy)  [k2smSBufs]
     bPV = bPF + k2smSBufs,         // P V from buffer b completed (both)      [k2smSBufs]
-    bOD = bPV + k2smSBufs,         // last P V completed (both)
-    bDR = bOD + 1,                 // drain after an abort (leader), one per issuer [2]
+    bOD = bPV + k2smSBufs,         // a pair's last P V completed (both)
+    bOE = bOD + 1,                 // O read by the epilogue (leader's copy, 8 arrivals)
+    bDR = bOE + 1,                 // drain after an abort (leader), one per issuer [2]
     kNumBars = bDR + 2
   };
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort
@@ -104,9 +106,9 @@ cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, bool varlen, int gri
                            cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, bool varlen, int grid,
                             cudaStream_t stream);
-// Dense head dim 128 on CTA pairs: `grid` = 2 x query pairs x key slices; p.tm_k has a 64-row
-// box.
-cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, int grid, cudaStream_t stream);
+// Dense head dim 128 on CTA pairs, persistent: `units` = query pairs x key slices, spread over as
+// many clusters of two CTAs as fit on the device; p.tm_k has a 64-row box.
+cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, int units, cudaStream_t stream);
 
 // Split-KV: slices per query pair the library picks when the caller passes num_splits <= 0, and
 // the merge of the slices' partial results (attn_splitkv.cu).  The pick minimises a simple cost
