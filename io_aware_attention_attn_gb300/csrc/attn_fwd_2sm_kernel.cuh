@@ -483,22 +483,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           }
         }
       } else {
+        // O / l in bf16 through this warp's 4 KB staging buffer, 64 columns at a time: each
+        // thread writes its row's 128 bytes (16-byte chunks XOR-swizzled by row, no bank
+        // conflicts), then every store instruction of the warp writes 4 whole 128-byte lines of
+        // 4 consecutive rows (a row per thread would touch 32 lines per instruction)
         const float inv_l = 1.f / l_exact;
-        uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);
+        const uint32_t stage = sbase + Lay::kOut + static_cast<uint32_t>(quarter) * 4096u;
+        uint8_t* stage_p = smem + Lay::kOut + quarter * 4096;
+        const int row0 = qrow0 + quarter * 32;  // first row of this warp
+        __nv_bfloat16* obase = p.o + (static_cast<size_t>(w.z) * static_cast<size_t>(p.N) +
+                                      static_cast<size_t>(row0)) * D;
         #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(o_col + cc * 32, o);
-          tmem_wait_ld_regs(o);
-          uint32_t pk[16];
+        for (int hcol = 0; hcol < 2; ++hcol) {
           #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
-          if (valid) {
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(o_col + hcol * 64 + cc * 32, o);
+            tmem_wait_ld_regs(o);
             #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              orow[cc * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) {
+              const int chunk = cc * 4 + q;  // 8 bf16 = 16 bytes
+              st_shared_v4(stage + lane * 128 + ((chunk ^ (lane & 7)) << 4),
+                           pack_bf16x2(u2f(o[8 * q + 0]) * inv_l, u2f(o[8 * q + 1]) * inv_l),
+                           pack_bf16x2(u2f(o[8 * q + 2]) * inv_l, u2f(o[8 * q + 3]) * inv_l),
+                           pack_bf16x2(u2f(o[8 * q + 4]) * inv_l, u2f(o[8 * q + 5]) * inv_l),
+                           pack_bf16x2(u2f(o[8 * q + 6]) * inv_l, u2f(o[8 * q + 7]) * inv_l));
+            }
           }
+          __syncwarp();
+          #pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3), chunk = lane & 7;
+            if (row0 + rr < seq_len) {
+              const uint4 val = *reinterpret_cast<const uint4*>(
+                  stage_p + rr * 128 + ((chunk ^ (rr & 7)) << 4));
+              *reinterpret_cast<uint4*>(obase + static_cast<size_t>(rr) * D + hcol * 64 +
+                                        chunk * 8) = val;
+            }
+          }
+          __syncwarp();  // the staging buffer is rewritten by the next half
         }
         if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
       }

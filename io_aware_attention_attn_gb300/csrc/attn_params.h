@@ -79,7 +79,8 @@ struct Fwd2smLayout {
   static constexpr int kQ = 0;                   // [2]: the current and the next query pair
   static constexpr int kK = kQ + 2 * kQBytes;
   static constexpr int kV = kK + k2smStagesK * kKBytes;
-  static constexpr int kBar = kV + k2smStagesV * kVBytes;
+  static constexpr int kOut = kV + k2smStagesV * kVBytes;  // epilogue staging [4 warps][4 KB]
+  static constexpr int kBar = kOut + 4 * 4096;
   enum {
     bQF = 0,                       // both CTAs' Q landed (leader's copy)   [2 Q buffers]
     bQE = bQF + 2,                 // Q buffer free: its S products done (both) [2]
