@@ -493,13 +493,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
         const int row0 = qrow0 + quarter * 32;  // first row of this warp
         __nv_bfloat16* obase = p.o + (static_cast<size_t>(w.z) * static_cast<size_t>(p.N) +
                                       static_cast<size_t>(row0)) * D;
+        // all of the row's O loads are issued before the first wait
+        uint32_t oa[32], ob[32], oc[32], od[32];
+        tmem_ld32(o_col + 0, oa);
+        tmem_ld32(o_col + 32, ob);
+        tmem_ld32(o_col + 64, oc);
+        tmem_ld32(o_col + 96, od);
+        tmem_wait_ld_regs(oa);
+        tmem_wait_ld_regs(ob);
+        tmem_wait_ld_regs(oc);
+        tmem_wait_ld_regs(od);
         #pragma unroll
         for (int hcol = 0; hcol < 2; ++hcol) {
           #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(o_col + hcol * 64 + cc * 32, o);
-            tmem_wait_ld_regs(o);
+            const uint32_t* o = hcol == 0 ? (cc == 0 ? oa : ob) : (cc == 0 ? oc : od);
             #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int chunk = cc * 4 + q;  // 8 bf16 = 16 bytes
