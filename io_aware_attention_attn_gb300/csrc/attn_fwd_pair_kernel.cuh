@@ -505,22 +505,41 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
       }
     } else if (n > 0 && ok) {
+      // O / l in bf16 through shared memory: every product that read Q_t has completed, so its
+      // tile is free, and each of this tile's warps stages its 32 rows there (16-byte chunks
+      // XOR-swizzled by row, no bank conflicts); every store instruction of the warp then writes
+      // whole 128-byte lines of consecutive rows (a row per thread would touch 32 lines)
       tc_fence_after();
       const float inv_l = 1.f / l_exact;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * D);
+      constexpr int kChunks = D / 8;  // 16-byte chunks per row
+      const uint32_t stage = sbase + Lay::kQ + t * Lay::kTile + quarter * (32 * D * 2);
+      const uint8_t* stage_p = smem + Lay::kQ + t * Lay::kTile + quarter * (32 * D * 2);
       #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(o_col + c * 32, o);
         tmem_wait_ld_regs(o);
-        uint32_t pk[16];
         #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
-        if (valid) {
-          #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            orow[c * 4 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = c * 4 + q;
+          st_shared_v4(stage + lane * (D * 2) + ((chunk ^ (lane & 7)) << 4),
+                       pack_bf16x2(u2f(o[8 * q + 0]) * inv_l, u2f(o[8 * q + 1]) * inv_l),
+                       pack_bf16x2(u2f(o[8 * q + 2]) * inv_l, u2f(o[8 * q + 3]) * inv_l),
+                       pack_bf16x2(u2f(o[8 * q + 4]) * inv_l, u2f(o[8 * q + 5]) * inv_l),
+                       pack_bf16x2(u2f(o[8 * q + 6]) * inv_l, u2f(o[8 * q + 7]) * inv_l));
+        }
+      }
+      __syncwarp();
+      const int row0 = qt * kBM + quarter * 32;  // this warp's first row within the sequence
+      __nv_bfloat16* obase = p.o + (static_cast<size_t>(z) * static_cast<size_t>(p.N) +
+                                    static_cast<size_t>(y0) + static_cast<size_t>(row0)) * D;
+      #pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        const int rr = i * (32 / kChunks) + lane / kChunks, chunk = lane % kChunks;
+        if (row0 + rr < seq_len) {
+          const uint4 val = *reinterpret_cast<const uint4*>(stage_p + rr * (D * 2) +
+                                                            ((chunk ^ (rr & 7)) << 4));
+          *reinterpret_cast<uint4*>(obase + static_cast<size_t>(rr) * D + chunk * 8) = val;
         }
       }
       if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
