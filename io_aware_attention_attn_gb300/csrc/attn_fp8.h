@@ -48,7 +48,8 @@ struct Fp8Layout {
   static constexpr int kQ = 0;             // Q_0, Q_1
   static constexpr int kK = kQ + 2 * kTile;
   static constexpr int kV = kK + kFp8StagesK * kTile;
-  static constexpr int kBar = kV + kFp8StagesV * kTile;
+  static constexpr int kOut = kV + kFp8StagesV * kTile;  // O staging: 8 warps x 32 rows x 256 B
+  static constexpr int kBar = kOut + 8 * 32 * 256;
   enum {
     bQ = 0,
     bKF = 1,

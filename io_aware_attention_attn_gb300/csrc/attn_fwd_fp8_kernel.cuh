@@ -327,29 +327,54 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
     }
     if (n > 0 && ok) ok = mbar_wait_warp(bar(Lay::bOD + t), 0, wc, 2, 9);
     if (n > 0 && ok) {
+      // O / l in bf16 through a staging area of this warp's own: 32 rows of 256 bytes, 16-byte
+      // chunks XOR-swizzled by row (no bank conflicts); every store instruction of the warp then
+      // writes two whole rows (a row per thread would touch 32 separate lines)
       tc_fence_after();
       const float l = (le[0] + le[1]) + (le[2] + le[3]);
       const bool valid = row < seq_len;
       const float mul = 1.f / (fv * l);  // sv_max / (kFp8PScale l)
-      const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
-                          static_cast<size_t>(valid ? row : 0);
-      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * 128);
+      const uint32_t stage = sbase + Lay::kOut + static_cast<uint32_t>(warp - 2) * (32 * 256);
+      const uint8_t* stage_p = smem + Lay::kOut + (warp - 2) * (32 * 256);
       #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(o_col + cc * 32, o);
-        tmem_wait_ld_regs(o);
-        if (valid) {
+      for (int cc = 0; cc < 4; cc += 2) {
+        uint32_t o[2][32];
+        tmem_ld32(o_col + cc * 32, o[0]);
+        tmem_ld32(o_col + cc * 32 + 32, o[1]);
+        tmem_wait_ld_regs(o[0]);
+        tmem_wait_ld_regs(o[1]);
+        #pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
           #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            orow[cc * 4 + q] =
-                make_uint4(pack_bf16x2(u2f(o[8 * q + 0]) * mul, u2f(o[8 * q + 1]) * mul),
-                           pack_bf16x2(u2f(o[8 * q + 2]) * mul, u2f(o[8 * q + 3]) * mul),
-                           pack_bf16x2(u2f(o[8 * q + 4]) * mul, u2f(o[8 * q + 5]) * mul),
-                           pack_bf16x2(u2f(o[8 * q + 6]) * mul, u2f(o[8 * q + 7]) * mul));
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = (cc + hh) * 4 + q;
+            const uint32_t* w = o[hh] + 8 * q;
+            st_shared_v4(stage + lane * 256 + ((chunk ^ (lane & 7)) << 4),
+                         pack_bf16x2(u2f(w[0]) * mul, u2f(w[1]) * mul),
+                         pack_bf16x2(u2f(w[2]) * mul, u2f(w[3]) * mul),
+                         pack_bf16x2(u2f(w[4]) * mul, u2f(w[5]) * mul),
+                         pack_bf16x2(u2f(w[6]) * mul, u2f(w[7]) * mul));
+          }
+      }
+      __syncwarp();
+      const int row0 = qt * kBM + quarter * 32;  // this warp's first row within the sequence
+      __nv_bfloat16* obase =
+          p.o + (static_cast<size_t>(z) * static_cast<size_t>(p.N) + static_cast<size_t>(row0)) *
+                    128;
+      #pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int rr = 2 * i + (lane >> 4), chunk = lane & 15;
+        if (row0 + rr < seq_len) {
+          const uint4 val =
+              *reinterpret_cast<const uint4*>(stage_p + rr * 256 + ((chunk ^ (rr & 7)) << 4));
+          *reinterpret_cast<uint4*>(obase + static_cast<size_t>(rr) * 128 + chunk * 8) = val;
         }
       }
-      if (valid) p.lse[grow] = (m2 + log2f(l)) * 0.69314718055994530942f;
+      if (valid) {
+        const size_t grow = static_cast<size_t>(z) * static_cast<size_t>(p.N) +
+                            static_cast<size_t>(row);
+        p.lse[grow] = (m2 + log2f(l)) * 0.69314718055994530942f;
+      }
     }
   }
   tc_fence_before();
