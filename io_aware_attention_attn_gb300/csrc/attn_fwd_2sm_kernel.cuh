@@ -283,15 +283,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           if (w.n == 0) continue;
           for (int j = 0; j < w.n; ++j, ++g) {
             const int b = g % NB, sv = g % SV;
-            if (!(ok = mbar_wait_spin_lane0(bar(Lay::bVF + sv),
+            if (!(ok = mbar_wait_warp(bar(Lay::bVF + sv),
                                             static_cast<uint32_t>(g / SV) & 1u, wc, 1, 6)))
               break;
-            if (!(ok = mbar_wait_spin_lane0(bar(Lay::bPF + b), static_cast<uint32_t>(g / NB) & 1u,
+            if (!(ok = mbar_wait_warp(bar(Lay::bPF + b), static_cast<uint32_t>(g / NB) & 1u,
                                             wc, 1, 5)))
               break;
             // the first product of a unit overwrites O: the previous unit's epilogue read it
             if (j == 0 && uq > 0 &&
-                !(ok = mbar_wait_spin_lane0(bar(Lay::bOE), static_cast<uint32_t>(uq - 1) & 1u, wc,
+                !(ok = mbar_wait_warp(bar(Lay::bOE), static_cast<uint32_t>(uq - 1) & 1u, wc,
                                             1, 8)))
               break;
             tc_fence_after();

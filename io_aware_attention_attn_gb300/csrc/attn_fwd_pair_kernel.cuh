@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= n_kv[t]) continue;
-        if (!(ok = mbar_wait_spin_warp(bar(Lay::bPF + t), static_cast<uint32_t>(j) & 1u, wc, 1, 5)))
+        if (!(ok = mbar_wait_warp(bar(Lay::bPF + t), static_cast<uint32_t>(j) & 1u, wc, 1, 5)))
           break;
         if (!v_ready) {
           if (!(ok = mbar_wait_warp(bar(Lay::bVF + sv),
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (j + 1 < n_kv[t]) {
           // S_t for the next key tile rewrites the columns P_t was read from: wait for P_t V_j
           if (!(ok = wait_k(j + 1))) break;
-          if (!(ok = mbar_wait_spin_warp(bar(Lay::bPV + t), static_cast<uint32_t>(j) & 1u, wc, 1, 7)))
+          if (!(ok = mbar_wait_warp(bar(Lay::bPV + t), static_cast<uint32_t>(j) & 1u, wc, 1, 7)))
             break;
           tc_fence_after();
           if (lane == 0) issue_s(t, j + 1);

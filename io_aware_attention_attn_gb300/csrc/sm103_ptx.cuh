@@ -107,9 +107,12 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, role, site)) != 0;
 }
 
-// Warp-uniform wait that polls with the non-suspending test instead of try_wait: for the MMA
-// issuer, whose every wait sits on the pipeline's critical chain, a suspended try_wait was seen to
-// wake a few hundred cycles after the phase completed.  Same limit and failure reporting.
+// Warp-uniform wait that polls with the non-suspending test instead of try_wait.  Which is faster
+// for an MMA issuer depends on the kernel: the backward issuers and the FP8 forward's measure a
+// little faster polling (a suspended try_wait can wake a few hundred cycles after the phase
+// completes), while in the bf16 forwards a polling issuer held back the completion of the
+// barrier it polled, whose last arrivals come from other warps and the peer CTA, by ~800 cycles
+// per key tile.  Same limit and failure reporting.
 __device__ __forceinline__ bool mbar_wait_spin_warp(uint32_t bar, uint32_t parity,
                                                     const WaitCtx& w, int role, int site) {
   bool done = mbar_test(bar, parity);
@@ -131,36 +134,6 @@ __device__ __forceinline__ bool mbar_wait_spin_warp(uint32_t bar, uint32_t parit
     }
     if (__any_sync(0xffffffffu, give_up)) return false;
   }
-}
-
-// Warp-uniform wait in which only lane 0 polls (with the non-suspending test) and the other
-// lanes take its answer: the polling warp then takes one issue slot per test instead of 32 lanes'
-// worth of shared-memory requests.  Same limit and failure reporting.
-__device__ __forceinline__ bool mbar_wait_spin_lane0(uint32_t bar, uint32_t parity,
-                                                     const WaitCtx& w, int role, int site) {
-  int state = 0;  // 1 done, 2 gave up
-  if (lane_id_is_zero()) {
-    if (mbar_test(bar, parity)) {
-      state = 1;
-    } else {
-      const unsigned long long t0 = global_timer_ns();
-      for (;;) {
-        #pragma unroll 1
-        for (int i = 0; i < 256 && state == 0; ++i)
-          if (mbar_test(bar, parity)) state = 1;
-        if (state) break;
-        if (*w.abort) {
-          state = 2;
-        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
-          atomicCAS(w.status, 0, kStatusTimeout | (role << 8) | (site << 16));
-          *w.abort = 1;
-          state = 2;
-        }
-        if (state) break;
-      }
-    }
-  }
-  return __shfl_sync(0xffffffffu, state, 0) == 1;
 }
 
 // Drain-only wait used while unwinding after an abort: ignores the abort flag, keeps the limit.
