@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(Lay::bSF + t), 1);
-      mbar_init(bar(Lay::bPF + t), 4 * 32);
+      mbar_init(bar(Lay::bPF + t), 4);
       mbar_init(bar(Lay::bPV + t), 1);
       mbar_init(bar(Lay::bOD + t), 1);
     }
@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(Lay::bPF + t));
+      __syncwarp();
+      if (lane_id_is_zero()) mbar_arrive(bar(Lay::bPF + t));
     }
     if (n > 0 && ok) ok = mbar_wait_warp(bar(Lay::bOD + t), 0, wc, 2, 9);
     if (n > 0 && ok) {
