@@ -155,7 +155,8 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   const uint64_t kv_heads = varlen ? static_cast<uint64_t>(Hkv) : static_cast<uint64_t>(B) * Hkv;
   if (encode_rows_map(&p.tm_q, q, d, N, q_heads) != CUDA_SUCCESS ||
       encode_rows_map(&p.tm_k, k, d, N, kv_heads, two_sm ? 64u : 128u) != CUDA_SUCCESS ||
-      encode_rows_map(&p.tm_v, v, d, N, kv_heads) != CUDA_SUCCESS)
+      encode_rows_map(&p.tm_v, v, d, N, kv_heads) != CUDA_SUCCESS ||
+      (two_sm && encode_rows_map(&p.tm_o, o, d, N, q_heads, 32u) != CUDA_SUCCESS))
     return ATTN_ERR_LAUNCH;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;

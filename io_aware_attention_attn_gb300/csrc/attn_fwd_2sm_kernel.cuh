@@ -483,22 +483,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           }
         }
       } else {
-        // O / l in bf16 through this warp's 4 KB staging buffer, 64 columns at a time: each
-        // thread writes its row's 128 bytes (16-byte chunks XOR-swizzled by row, no bank
-        // conflicts), then every store instruction of the warp writes 4 whole 128-byte lines of
-        // 4 consecutive rows (a row per thread would touch 32 lines per instruction)
+        // O / l in bf16, staged in this warp's 8 KB area as two 64-column halves of its 32 rows
+        // (16-byte chunks XOR-swizzled by row: the tensor map's 128-byte swizzle, and no bank
+        // conflicts), then written by two TMA stores that run on while the warp starts the next
+        // unit; the map clips rows past the end of the sequence.  The area is rewritten one unit
+        // later, once those stores have read it.
         const float inv_l = 1.f / l_exact;
-        const uint32_t stage = sbase + Lay::kOut + static_cast<uint32_t>(quarter) * 4096u;
-        uint8_t* stage_p = smem + Lay::kOut + quarter * 4096;
+        const uint32_t stage = sbase + Lay::kOut + static_cast<uint32_t>(quarter) * 8192u;
         const int row0 = qrow0 + quarter * 32;  // first row of this warp
-        __nv_bfloat16* obase = p.o + (static_cast<size_t>(w.z) * static_cast<size_t>(p.N) +
-                                      static_cast<size_t>(row0)) * D;
         // all of the row's O loads are issued before the first wait
         uint32_t oa[32], ob[32], oc[32], od[32];
         tmem_ld32(o_col + 0, oa);
         tmem_ld32(o_col + 32, ob);
         tmem_ld32(o_col + 64, oc);
         tmem_ld32(o_col + 96, od);
+        if (lane == 0) bulk_wait_group_read0();  // the previous unit's stores have read the area
+        __syncwarp();
         tmem_wait_ld_regs(oa);
         tmem_wait_ld_regs(ob);
         tmem_wait_ld_regs(oc);
@@ -511,25 +511,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
             #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int chunk = cc * 4 + q;  // 8 bf16 = 16 bytes
-              st_shared_v4(stage + lane * 128 + ((chunk ^ (lane & 7)) << 4),
+              st_shared_v4(stage + hcol * 4096 + lane * 128 + ((chunk ^ (lane & 7)) << 4),
                            pack_bf16x2(u2f(o[8 * q + 0]) * inv_l, u2f(o[8 * q + 1]) * inv_l),
                            pack_bf16x2(u2f(o[8 * q + 2]) * inv_l, u2f(o[8 * q + 3]) * inv_l),
                            pack_bf16x2(u2f(o[8 * q + 4]) * inv_l, u2f(o[8 * q + 5]) * inv_l),
                            pack_bf16x2(u2f(o[8 * q + 6]) * inv_l, u2f(o[8 * q + 7]) * inv_l));
             }
           }
-          __syncwarp();
-          #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = 4 * i + (lane >> 3), chunk = lane & 7;
-            if (row0 + rr < seq_len) {
-              const uint4 val = *reinterpret_cast<const uint4*>(
-                  stage_p + rr * 128 + ((chunk ^ (rr & 7)) << 4));
-              *reinterpret_cast<uint4*>(obase + static_cast<size_t>(rr) * D + hcol * 64 +
-                                        chunk * 8) = val;
-            }
-          }
-          __syncwarp();  // the staging buffer is rewritten by the next half
+        }
+        fence_proxy_async_smem();  // the generic-proxy writes above, before the async-proxy reads
+        __syncwarp();
+        if (lane == 0 && row0 < seq_len) {
+          tma_store_3d(&p.tm_o, stage, 0, row0, w.z);
+          tma_store_3d(&p.tm_o, stage + 4096, 64, row0, w.z);
+          bulk_commit_group();
         }
         if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
       }
@@ -539,6 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       if (lane == 0) mbar_arrive_cluster(lbar(Lay::bOE));
       ++uq;
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's O stores have completed
   }
   tc_fence_before();
   cluster_sync_all();  // no MMA, copy or remote arrival of either CTA is still in flight

@@ -20,6 +20,7 @@ struct FwdParams {
   CUtensorMap tm_q;          // 3-D maps {d, rows, heads}, box {64, 128, 1}, 128-byte swizzle
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;          // O as {d, rows, heads}, box {64, 32, 1}: two-SM epilogue stores
   __nv_bfloat16* o;
   float* lse;
   const int* cu_seqlens;     // packed layout only
@@ -79,8 +80,10 @@ struct Fwd2smLayout {
   static constexpr int kQ = 0;                   // [2]: the current and the next query pair
   static constexpr int kK = kQ + 2 * kQBytes;
   static constexpr int kV = kK + k2smStagesK * kKBytes;
-  static constexpr int kOut = kV + k2smStagesV * kVBytes;  // epilogue staging [4 warps][4 KB]
-  static constexpr int kBar = kOut + 4 * 4096;
+  // epilogue staging [4 warps][2 halves][32 rows x 128 bytes], 1024-byte aligned: the TMA
+  // stores of O read it in the 128-byte swizzle
+  static constexpr int kOut = kV + k2smStagesV * kVBytes;
+  static constexpr int kBar = kOut + 4 * 8192;
   enum {
     bQF = 0,                       // both CTAs' Q landed (leader's copy)   [2 Q buffers]
     bQE = bQF + 2,                 // Q buffer free: its S products done (both) [2]
@@ -100,6 +103,8 @@ struct Fwd2smLayout {
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynBytes = kBytes + 1024;
 };
+static_assert(Fwd2smLayout::kOut % 1024 == 0, "O staging must sit on the swizzle atom");
+
 static_assert(Fwd2smLayout::kDynBytes <= 232448, "two-SM kernel exceeds 227 KB shared memory");
 
 // Host launchers (one translation unit per head dimension).
