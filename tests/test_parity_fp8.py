@@ -105,3 +105,17 @@ def test_fp8_full_size_sampled_heads(causal):
     for b, h in heads:
         check_fp8(o[b, h], lse[b, h], o_ref[b, h], lse_ref[b, h], bounds[(b, h)],
                   f"{w.name} ({b},{h})")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_many_units_per_cluster(causal):
+    # 3 query pairs x 96 heads = 288 units of 256 query rows, more than the GPU holds at once;
+    # the last pair of every head is ragged (its second tile ends at row 700).  Every head is
+    # compared.
+    w = configs.custom(818 + int(causal), 2, 48, 700, 128, causal)
+    q, k, v, o, lse = run_fp8(w)
+    heads = [(b, h) for b in range(2) for h in range(48)]
+    o_ref, lse_ref, bounds = reference(q, k, v, causal, w.scale, heads)
+    for b, h in heads:
+        check_fp8(o[b, h], lse[b, h], o_ref[b, h], lse_ref[b, h], bounds[(b, h)],
+                  f"{w.name} ({b},{h})")
