@@ -146,12 +146,14 @@ def cpu_cores() -> int:
 
 def oracle_sample(w, q, k, v, target_s: float, max_rows: int | None = None):
     """Time the float64 oracle on query rows of the workload (head-major, from head (0, 0))
-    until about ``target_s`` seconds have passed; returns (TFLOPS, rows, seconds)."""
+    until about ``target_s`` seconds have passed (at least one block of rows); returns
+    (TFLOPS, rows, seconds)."""
     from oracle import attention as orc
     N = w.N
     rows_done, flops, t_total = 0, 0.0, 0.0
     step = 128
-    while t_total < target_s and rows_done < (max_rows or N * w.B * w.H):
+    limit = max_rows or N * w.B * w.H
+    while rows_done == 0 or (t_total < target_s and rows_done < limit):  # at least one block
         r0 = rows_done % N
         hidx = rows_done // N
         b, h = divmod(hidx % (w.B * w.H), w.H)
