@@ -25,7 +25,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_gloo():
     port = 29500 + os.getpid() % 1000
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this (threaded) process
         out = m.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         assert dict(out) == {0: 15.0, 1: 15.0}
