@@ -1,0 +1,86 @@
+"""Properties of the persistent forward's work distribution, checked on the host.
+
+The head-dim-128 forward runs G clusters that each walk the work units c, 2G-1-c, 2G+c, 4G-1-c,
+... (rounds of G units, alternately forward and backward), and splits a query pair's key tiles
+into slices of ceil(n / S) tiles.  These tests restate those two formulas as the kernel states
+them and check what the kernel relies on: every unit is taken by exactly one cluster, each
+cluster's units come in increasing rounds, the slices of a pair cover its key tiles exactly once,
+and a causal pair's key range reaches the diagonal of its last row.  The slice-count choice made
+by the library is checked through the C ABI (no GPU needed).
+"""
+import pytest
+
+from io_aware_attention_attn_gb300 import attn
+
+BM = BN = 128
+
+
+def next_unit(k, c, G):
+    return k * G + ((G - 1 - c) if (k & 1) else c)
+
+
+def walk(c, G, n_units):
+    k, u = 0, c
+    out = []
+    while u < n_units:
+        out.append(u)
+        k += 1
+        u = next_unit(k, c, G)
+    return out
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 7, 64, 75, 76])
+@pytest.mark.parametrize("n_units", [1, 5, 75, 76, 77, 151, 152, 1024, 1500])
+def test_every_unit_exactly_once(G, n_units):
+    seen = {}
+    for c in range(G):
+        units = walk(c, G, n_units)
+        assert units == sorted(units)  # rounds in order: Q buffers and phases advance monotonically
+        for u in units:
+            assert u not in seen, (u, c, seen.get(u))
+            seen[u] = c
+    assert sorted(seen) == list(range(n_units))
+    # balance: no cluster takes more than one unit beyond another
+    counts = [len(walk(c, G, n_units)) for c in range(G)]
+    assert max(counts) - min(counts) <= 1
+
+
+def key_slices(n_full, n_splits):
+    chunk = (n_full + n_splits - 1) // n_splits
+    out = []
+    for split in range(n_splits):
+        kb = split * chunk
+        n = max(0, min(kb + chunk, n_full) - kb)
+        out.append((kb, n))
+    return out
+
+
+@pytest.mark.parametrize("n_full", [1, 2, 3, 7, 8, 31, 32, 64, 128])
+@pytest.mark.parametrize("n_splits", [1, 2, 3, 5, 8, 16])
+def test_key_slices_cover_once(n_full, n_splits):
+    covered = []
+    for kb, n in key_slices(n_full, n_splits):
+        covered.extend(range(kb, kb + n))
+    assert covered == list(range(n_full))
+
+
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 255, 256, 300, 1000, 4096])
+def test_causal_pair_reaches_its_diagonal(N):
+    n_keytiles = (N + BN - 1) // BN
+    n_pairs = (N + 2 * BM - 1) // (2 * BM)
+    for pt in range(n_pairs):
+        n_full = min(n_keytiles, 2 * pt + 2)
+        last_row = min(N, (2 * pt + 2) * BM) - 1
+        # the key tiles cover every key <= the pair's last row, and stay inside the sequence
+        assert n_full * BN > last_row
+        assert (n_full - 1) * BN < N
+
+
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 8192, 128), (1, 1, 256, 64), (2, 32, 4096, 128),
+                                     (1, 4, 16384, 64), (1, 1, 100, 128)])
+def test_slice_count_is_within_key_tiles(B, H, N, d):
+    s = attn.splitkv_slices(B, H, N, d, 0)
+    key_tiles = (N + BN - 1) // BN
+    assert 1 <= s <= max(1, key_tiles)
+    # an explicit request is clamped to the key tiles, never raised
+    assert attn.splitkv_slices(B, H, N, d, 3) == min(3, key_tiles)
