@@ -8,9 +8,11 @@
  * "merged into a logsumexp"; CS336 GPU/attention notes, "Online softmax 回顾", for the merge).
  *
  * Conventions shared by every entry point:
- *   - All tensor pointers are DEVICE pointers owned by the caller.  The library allocates no
- *     device memory (the fused kernel uses on-chip shared and tensor memory only; the unfused
- *     comparison path uses a caller-provided workspace).
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  No call allocates device
+ *     memory (the fused kernel uses on-chip shared and tensor memory only; the unfused
+ *     comparison path uses a caller-provided workspace).  The one piece of device memory the
+ *     library holds is a file-scope array of ATTN_NOALLOC_SCRATCH_BYTES (64 MiB), the scratch of
+ *     attn_fwd_unfused_noalloc, which every GPU that loads the library keeps until exit.
  *   - Element types: q, k, v, o are bfloat16 (passed as void*); lse is float32;
  *     cu_seqlens is int32.
  *   - Dense layout (cu_seqlens == NULL): q, k, v, o are [B, H, N, d] contiguous, d innermost;
@@ -260,8 +262,10 @@ ATTN_API size_t attn_fwd_unfused_workspace_bytes(int B, int H, int N, int d);
  *   Arguments as attn_fwd_unfused (dense layout only), without cu_seqlens and the workspace.
  *   Returns ATTN_ERR_SCRATCH_LIMIT when attn_fwd_unfused_workspace_bytes(B, H, N, d) exceeds
  *   ATTN_NOALLOC_SCRATCH_BYTES, before touching the GPU.
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
- *   device current); make that first call before any stream capture.
+ *   Every call looks up the array's device address (cudaGetSymbolAddress, with the calling
+ *   device current); nothing is cached, so a device reset between calls leaves no stale address.
+ *   The first call in a context loads the module there; make that first call before any stream
+ *   capture.
  *   All calls share the array and it keeps the last call's contents (nothing in it needs to start
  *   at zero); calls whose work overlaps on the GPU, e.g. on two streams, race on it.
  */

@@ -36,7 +36,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_ok[kMaxDevices];          // 0 unknown, 1 sm_103, 2 other
-std::atomic<int*> g_status_ptr[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -98,17 +97,12 @@ int check_device() {
   return st == 1 ? 0 : ATTN_ERR_DEVICE;
 }
 
+// Device address of the status word in the current context.  Looked up on every call, not cached
+// per device: after a device reset or a new context the module may load at another address.
 int* status_word() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
-  if (!p) {
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_attn_status) != cudaSuccess) return nullptr;
-    p = static_cast<int*>(addr);
-    g_status_ptr[dev].store(p, std::memory_order_release);
-  }
-  return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_attn_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(addr);
 }
 
 // Shared validation of attn_fwd / attn_fwd_unfused.  Sets *empty when there is nothing to do.

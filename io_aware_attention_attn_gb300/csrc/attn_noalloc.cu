@@ -9,14 +9,15 @@
 // the process exits.
 //
 // In host code the array's name is only a host-side stand-in, never a device address: its device
-// address is looked up once per device with cudaGetSymbolAddress (on the first call on that device,
-// with that device current) and passed to the kernels as their workspace pointer.
+// address is looked up with cudaGetSymbolAddress on every call, with the calling device current,
+// and passed to the kernels as their workspace pointer.  Nothing is cached between calls, so a
+// device reset or a context torn down and re-created in between (which may load the module at
+// another address) cannot leave a stale pointer behind.  The first call in a context loads the
+// module there; make that first call before any stream capture.
 //
 // Every call shares the array and it keeps the previous call's contents.  Nothing in it has to
 // start at zero: the three kernels write every element of S, P and 1/l that they later read.
 // Calls whose work overlaps on the GPU (for example on two streams) race on the array.
-#include <atomic>
-
 #include "attn_gb300.h"
 #include "attn_params.h"
 
@@ -25,20 +26,11 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-
-// Device address of the scratch array on the current device (set up on first use).
+// Device address of the scratch array in the current context (looked up on every call).
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_LAUNCH;
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return ATTN_ERR_LAUNCH;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
-  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return ATTN_ERR_LAUNCH;
   *out = p;
   return ATTN_OK;
 }

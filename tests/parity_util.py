@@ -1,19 +1,35 @@
-"""Shared helpers for the GPU parity tests: device transfer and the tolerance check.
+"""Shared helpers for the GPU parity tests: device transfer, the tolerance checks and the record
+of the error each case achieved.
 
 Tolerance (stated for the attention forward): O within max abs error 1e-2 and mean abs error
-1e-3 of the float64 oracle, LSE within 1e-3 absolute.  O is a bf16 output, and a correctly
-rounded bf16 value can sit up to half a bf16 spacing from the exact result (0.0156 for |O| in
-[4, 8)); the max-abs bound is therefore applied to the kernel's error on top of that unavoidable
-output rounding: |O_gpu - O_ref| <= 1e-2 + half_ulp_bf16(O_ref).
+1e-3 of the float64 oracle, LSE within 1e-3 absolute.  O is a bf16 output.  Below |O| = 2 a
+correctly rounded bf16 value sits within 2^-8 of the exact result, so the literal 1e-2 applies
+there unchanged.  From |O| = 2 up, half a bf16 spacing (2^-8 * 2^e) reaches 0.0078 and then
+0.0156, so 1e-2 cannot hold even for a perfectly rounded output; there the bound is applied to
+the kernel's error on top of that unavoidable rounding: |O_gpu - O_ref| <= 1e-2 + half_ulp(O_ref).
+
+Every check also measures the kernel's own error against the correctly rounded reference
+RNE_bf16(O_ref) in bf16 spacings (0 = the same bf16 value, 1 = a neighbour) and appends its
+statistics to RESULTS.  The test session prints them at the end and, when the environment
+variable ATTN_PARITY_LOG names a file, writes them there as JSON lines.
 """
 import numpy as np
 import torch
 
+from gen import inputs
 from io_aware_attention_attn_gb300 import accounting as acc
 
 O_MAX_ABS = 1e-2
 O_MEAN_ABS = 1e-3
 LSE_ABS = 1e-3
+# magnitude from which half a bf16 spacing (2^-8 * 2^e) is no longer small beside 1e-2
+O_WIDEN_FROM = 2.0
+
+RESULTS: list = []
+
+
+def record(kind: str, what: str, stats: dict) -> None:
+    RESULTS.append({"kind": kind, "case": what, **stats})
 
 
 def to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -26,19 +42,33 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
+def rne_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 -> the nearest bf16 value (ties to even), as float64."""
+    bits = inputs.f64_to_bf16_bits(np.asarray(x, dtype=np.float64)).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
 def check(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray,
           what: str = "") -> dict:
-    """Element-wise comparison; raises AssertionError with a summary on failure."""
+    """Element-wise comparison; records the achieved error, raises AssertionError on failure."""
     assert o_gpu.shape == o_ref.shape and lse_gpu.shape == lse_ref.shape, what
     assert np.isfinite(o_gpu).all(), f"{what}: non-finite O"
     assert np.isfinite(lse_gpu).all(), f"{what}: non-finite LSE"
     err = np.abs(o_gpu - o_ref)
-    tol = O_MAX_ABS + acc.bf16_half_ulp(o_ref)
+    big = np.abs(o_ref) >= O_WIDEN_FROM
+    tol = np.where(big, O_MAX_ABS + acc.bf16_half_ulp(o_ref), O_MAX_ABS)
     bad = err > tol
+    ulps = np.abs(o_gpu - rne_bf16(o_ref)) / (2.0 * acc.bf16_half_ulp(o_ref))
     lerr = np.abs(lse_gpu - lse_ref)
     stats = {"o_max_abs": float(err.max()), "o_mean_abs": float(err.mean()),
-             "o_over_1e-2": int((err > O_MAX_ABS).sum()), "lse_max_abs": float(lerr.max()),
+             "o_over_1e-2": int((err > O_MAX_ABS).sum()),
+             "o_over_1e-2_below_2": int(((err > O_MAX_ABS) & ~big).sum()),
+             "n_abs_o_ge_2": int(big.sum()),
+             "o_max_ulps_from_rounded": float(ulps.max()),
+             "o_frac_correctly_rounded": float((ulps == 0).mean()),
+             "lse_max_abs": float(lerr.max()), "lse_mean_abs": float(lerr.mean()),
              "n": int(err.size)}
+    record("fwd", what, stats)
     assert not bad.any(), f"{what}: {int(bad.sum())} O values over tolerance; {stats}"
     assert err.mean() <= O_MEAN_ABS, f"{what}: mean abs error {err.mean()}; {stats}"
     assert lerr.max() <= LSE_ABS, f"{what}: LSE error {lerr.max()}; {stats}"
@@ -77,6 +107,7 @@ def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, bound: np.ndarray, what: st
     tol = acc.bf16_half_ulp(g_ref) + GRAD_C * bound
     stats = {"max_abs": float(err.max()), "max_err_over_tol": float((err / tol).max()),
              "mean_abs": float(err.mean()), "mean_bound": float(bound.mean()), "n": int(err.size)}
+    record("bwd", what, stats)
     assert (err <= tol).all(), f"{what}: {int((err > tol).sum())} entries over tolerance; {stats}"
     assert err.mean() <= GRAD_MEAN_C * bound.mean(), f"{what}: mean error; {stats}"
     return stats
@@ -98,8 +129,10 @@ def check_fp8(o_gpu, lse_gpu, o_ref, lse_ref, a_bound, what=""):
     err = np.abs(o_gpu - o_ref)
     tol = acc.bf16_half_ulp(o_ref) + FP8_C * a_bound
     stats = {"o_max_abs": float(err.max()), "max_err_over_tol": float((err / tol).max()),
+             "max_err_over_a": float(((err - acc.bf16_half_ulp(o_ref)).clip(0) / a_bound).max()),
              "mean_over_bound": float(err.mean() / a_bound.mean()),
              "lse_max_abs": float(np.abs(lse_gpu - lse_ref).max())}
+    record("fp8", what, stats)
     assert (err <= tol).all(), f"{what}: {int((err > tol).sum())} O values over tolerance; {stats}"
     assert err.mean() <= FP8_MEAN_C * a_bound.mean(), f"{what}: mean error; {stats}"
     assert np.abs(lse_gpu - lse_ref).max() <= LSE_ABS, f"{what}: LSE; {stats}"

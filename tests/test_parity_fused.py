@@ -173,7 +173,15 @@ def _sample_rows(N, rng, extra=64):
     return rows
 
 
-@pytest.mark.parametrize("index", [2, 3, 4])
+def test_full_size_workload_2_every_element():
+    """B=4, H=16, N=1024, d=64 causal in full: all 64 heads x 1024 rows against the oracle."""
+    w = configs.WORKLOADS[2]
+    q, k, v, o, lse = run_dense(w)
+    o_ref, lse_ref = orc.attention_dense(q, k, v, w.causal, w.scale)
+    check(to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, w.name + " (all rows)")
+
+
+@pytest.mark.parametrize("index", [3, 4])
 def test_full_size_dense_workload(index):
     w = configs.WORKLOADS[index]
     q, k, v, o, lse = run_dense(w)
