@@ -44,14 +44,25 @@ METRIC = "fused attention fwd TFLOPS at d=128 N=4096; % of BF16 tensor peak"
 L2_FLUSH_BYTES = 256 << 20
 
 
-# the files that make up the fused kernel the headline times (head dim 128, dense: the two-SM
-# kernel): a profile taken on other contents is stale
-FUSED_SOURCES = ("attn_fwd_2sm_kernel.cuh", "attn_params.h", "sm103_ptx.cuh", "attn_fwd_2sm.cu")
+# the files that make up each fused forward kernel: a profile taken on other contents is stale
+KERNEL_SOURCES = {
+    "attn_fwd_2sm_kernel": ("attn_fwd_2sm_kernel.cuh", "attn_params.h", "sm103_ptx.cuh",
+                            "attn_fwd_2sm.cu"),
+    "attn_fwd_pair_kernel": ("attn_fwd_pair_kernel.cuh", "attn_params.h", "sm103_ptx.cuh",
+                             "attn_fwd_d64.cu", "attn_fwd_d128.cu"),
+}
+FUSED_SOURCES = KERNEL_SOURCES["attn_fwd_2sm_kernel"]
 
 
-def sources_digest() -> str:
+def kernel_for(w) -> str:
+    """The forward kernel the library runs for a workload (dense head dim 128 on CTA pairs;
+    head dim 64 and packed batches on the two-tile kernel)."""
+    return "attn_fwd_2sm_kernel" if (w.d == 128 and not w.varlen) else "attn_fwd_pair_kernel"
+
+
+def sources_digest(files=FUSED_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in FUSED_SOURCES:
+    for f in files:
         h.update(open(os.path.join(ROOT, "io_aware_attention_attn_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -66,15 +77,28 @@ def measured_peaks() -> dict:
             "_source": "fallback"}
 
 
+def _profile_lookup(pattern: str, digest: str):
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for m in re.finditer(pattern + r":\s*([\d.]+)\s+sources:\s*(\w+)", open(f).read()):
+            if m.group(2) == digest:
+                return m.group(1)
+    return None
+
+
 def profiled_traffic(kernel_tag: str):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
-    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
-        text = open(f).read()
-        m = re.search(r"traffic_bytes_per_launch\[" + re.escape(kernel_tag) +
-                      r"\]:\s*(\d+)\s+sources:\s*(\w+)", text)
-        if m and m.group(2) == sources_digest():
-            return int(m.group(1))
-    return None
+    v = _profile_lookup(r"traffic_bytes_per_launch\[" + re.escape(kernel_tag) + r"\]",
+                        sources_digest())
+    return int(v) if v is not None else None
+
+
+def profiled_tensor_pipe(w):
+    """ncu sm__pipe_tensor_cycles_active (percent of peak) of the kernel that serves workload
+    ``w``, from a committed single-launch summary taken on that kernel's current sources."""
+    kern = kernel_for(w)
+    v = _profile_lookup(r"tensor_pipe_active\[" + re.escape(kern) + "@" + re.escape(w.name) +
+                        r"\]", sources_digest(KERNEL_SOURCES[kern]))
+    return float(v) if v is not None else None
 
 
 class ClockSampler:
@@ -132,7 +156,7 @@ def max_over_ranks(value: float, dist, device=None) -> float:
     return float(t.item())
 
 
-def cpu_cores() -> int:
+def blas_threads():
     try:
         import threadpoolctl
         info = threadpoolctl.threadpool_info()
@@ -141,29 +165,61 @@ def cpu_cores() -> int:
             return int(max(blas))
     except Exception:
         pass
-    return os.cpu_count() or 1
+    return None
+
+
+def cpu_cores() -> int:
+    """Threads the oracle's float64 matmuls use (the BLAS pool), else the host's core count."""
+    return blas_threads() or os.cpu_count() or 1
+
+
+def cpu_info() -> dict:
+    return {"cores": cpu_cores(), "host_cpu_count": os.cpu_count(),
+            "blas_threads": blas_threads()}
+
+
+def _head_slices(w, q, k, v):
+    """(q, k, v) of each attention problem of the workload, head-major from the first head:
+    dense [B, H, N, d] gives one per (b, h); packed [H, T, d] one per (h, sequence)."""
+    if not w.varlen:
+        for i in range(w.B * w.H):
+            b, h = divmod(i, w.H)
+            yield q[b, h], k[b, h], v[b, h]
+    else:
+        cu = w.cu_seqlens()
+        for h in range(w.H):
+            for s_ in range(len(cu) - 1):
+                a, e = int(cu[s_]), int(cu[s_ + 1])
+                if e > a:
+                    yield q[h, a:e], k[h, a:e], v[h, a:e]
 
 
 def oracle_sample(w, q, k, v, target_s: float, max_rows: int | None = None):
-    """Time the float64 oracle on query rows of the workload (head-major, from head (0, 0))
-    until about ``target_s`` seconds have passed (at least one block of rows); returns
+    """Time the float64 oracle on query rows of the workload (problem by problem from the first
+    head) until about ``target_s`` seconds have passed (at least one block of rows); returns
     (TFLOPS, rows, seconds)."""
     from oracle import attention as orc
-    N = w.N
     rows_done, flops, t_total = 0, 0.0, 0.0
     step = 128
-    limit = max_rows or N * w.B * w.H
+    limit = max_rows or w.H * w.total_tokens()
+    problems = _head_slices(w, q, k, v)
+    cur, r0 = None, 0
     while rows_done == 0 or (t_total < target_s and rows_done < limit):  # at least one block
-        r0 = rows_done % N
-        hidx = rows_done // N
-        b, h = divmod(hidx % (w.B * w.H), w.H)
-        rows = np.arange(r0, min(N, r0 + step))
+        if cur is None or r0 >= cur[0].shape[0]:
+            try:
+                cur, r0 = next(problems), 0
+            except StopIteration:
+                break
+        qq, kk, vv = cur
+        L = qq.shape[0]
+        rows = np.arange(r0, min(L, r0 + step))
         t0 = time.perf_counter()
-        orc.attention_head_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
+        orc.attention_head_rows(qq, kk, vv, rows, w.causal, w.scale)
         t_total += time.perf_counter() - t0
-        vis = [(int(r) + 1) if w.causal else N for r in rows]
+        vis = [(int(r) + 1) if w.causal else L for r in rows]
         flops += sum(4.0 * x * w.d for x in vis)
         rows_done += len(rows)
+        r0 += len(rows)
         step = min(step * 2, 1024)
     return flops / t_total / 1e12, rows_done, t_total
 
@@ -172,7 +228,7 @@ def run_reference(args, w, rank, world):
     if rank != 0:
         return
     q, k, v, _ = w.make()
-    cores = cpu_cores()
+    cores = cpu_info()
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(w, q, k, v, per_step)
@@ -190,9 +246,9 @@ def run_reference(args, w, rank, world):
         "data": "synthetic (seeded splitmix64/Box-Muller, bf16-rounded)",
         "config": {**w.describe(), "l2": "n/a (host)"},
         "impl": "reference",
-        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                         "sample": f"float64 oracle, {rows} query rows (head-major from head "
-                                   f"(0,0)) of {w.name} over {args.steps} steps"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", **cores, "kind": "oracle",
+                         "sample": f"float64 oracle, {rows} query rows (problem by problem "
+                                   f"from the first head) of {w.name} over {args.steps} steps"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -208,20 +264,23 @@ def run_ours(args, w, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     attn.lib()
-    q_np, k_np, v_np, _ = w.make()
+    q_np, k_np, v_np, cu_np = w.make()
 
     def to_dev(x):
         return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
 
     q, k, v = to_dev(q_np), to_dev(k_np), to_dev(v_np)
+    cu = torch.from_numpy(cu_np).to(dev) if w.varlen else None
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    flops = acc.attention_flops(w.H, [w.N] * w.B, w.d, w.causal)
+    lengths = [int(x) for x in np.diff(cu_np)] if w.varlen else [w.N] * w.B
+    flops = acc.attention_flops(w.H, lengths, w.d, w.causal)
 
     def step():
-        attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+        attn.attn_fwd(q, k, v, cu_seqlens=cu, causal=w.causal, scale=w.scale, out=o, lse=lse,
+                      stream=stream)
 
     def barrier():
         if dist is not None:
@@ -255,9 +314,13 @@ def run_ours(args, w, rank, world, dist):
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic("attn_fwd_kernel"),
+                "frac": achieved / peak,
+                "traffic": profiled_traffic("attn_fwd_kernel") if w is configs.WORKLOADS[
+                    configs.HEADLINE] else None,
                 "peak_source": f"{peaks['_source']} bf16 burst (cuBLAS)",
-                "algorithmic_bytes": acc.attention_ideal_bytes(w.H, w.B * w.N, w.d)}
+                "tensor_pipe_active": profiled_tensor_pipe(w),
+                "kernel": kernel_for(w),
+                "algorithmic_bytes": acc.attention_ideal_bytes(w.H, w.total_tokens(), w.d)}
 
     # ---- end to end through the public API: pinned host -> device, forward, device -> host.
     # Every step copies its own Q, K, V in and its O and LSE out; steps are pipelined over two
@@ -269,9 +332,13 @@ def run_ours(args, w, rank, world, dist):
         n_e2e = max(3, min(args.steps, 50))
         h_in = [[torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
                  for x in (q_np, k_np, v_np)] for _ in range(2)]
+        if w.varlen:
+            for hb in h_in:
+                hb.append(torch.from_numpy(cu_np).pin_memory())
         h_out = [(torch.empty(o.shape, dtype=torch.bfloat16).pin_memory(),
                   torch.empty(lse.shape, dtype=torch.float32).pin_memory()) for _ in range(2)]
-        d_in = [[torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)] for _ in range(2)]
+        d_in = [[torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)] +
+                ([torch.empty_like(cu)] if w.varlen else []) for _ in range(2)]
         d_out = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
         s_h2d = torch.cuda.Stream(dev)
         s_d2h = torch.cuda.Stream(dev)
@@ -299,7 +366,8 @@ def run_ours(args, w, rank, world, dist):
                 stream.wait_event(ev_in[b])
                 if used[b]:
                     stream.wait_event(ev_out[b])  # the buffer's previous outputs left the device
-                attn.attn_fwd(d_in[b][0], d_in[b][1], d_in[b][2], causal=w.causal,
+                attn.attn_fwd(d_in[b][0], d_in[b][1], d_in[b][2],
+                              cu_seqlens=d_in[b][3] if w.varlen else None, causal=w.causal,
                               scale=w.scale, out=d_out[b][0], lse=d_out[b][1], stream=stream)
                 ev_done[b].record(stream)
                 used[b] = True
@@ -316,7 +384,9 @@ def run_ours(args, w, rank, world, dist):
                 dq_ = h_in[0][0].to(dev, non_blocking=True)
                 dk_ = h_in[0][1].to(dev, non_blocking=True)
                 dv_ = h_in[0][2].to(dev, non_blocking=True)
-                oo, ll = attn.attn_fwd(dq_, dk_, dv_, causal=w.causal, scale=w.scale)
+                dc_ = h_in[0][3].to(dev, non_blocking=True) if w.varlen else None
+                oo, ll = attn.attn_fwd(dq_, dk_, dv_, cu_seqlens=dc_, causal=w.causal,
+                                       scale=w.scale)
                 h_out[0][0].copy_(oo, non_blocking=True)
                 h_out[0][1].copy_(ll, non_blocking=True)
 
@@ -337,7 +407,7 @@ def run_ours(args, w, rank, world, dist):
                               o.view(torch.int16).cpu().numpy()):
             raise RuntimeError("end-to-end output differs from the device-resident run")
         e2e = {"value": flops * n_e2e * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-               "h2d_bytes_per_step": 3 * q.numel() * 2,
+               "h2d_bytes_per_step": 3 * q.numel() * 2 + (cu.numel() * 4 if w.varlen else 0),
                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4, "steps": n_e2e,
                "pipelined": "two device buffers; H2D of step i+1 and D2H of step i-1 overlap step i",
                "serial_value": flops * n_e2e * world / (s_ms * 1e-3) / 1e12}
@@ -345,7 +415,7 @@ def run_ours(args, w, rank, world, dist):
 
     # ---- unfused three-kernel comparison path (memory wall)
     unfused = None
-    if not args.no_unfused:
+    if not args.no_unfused and not w.varlen:  # the comparison path takes dense batches only
         try:
             need = attn.unfused_workspace_bytes(w.B, w.H, w.N, w.d)
             ws = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -446,7 +516,7 @@ def run_ours(args, w, rank, world, dist):
     # ---- FP8 (E4M3) forward on the same shape: quantize once, then time the FP8 kernel; the
     # quantization of Q, K and V (three launches) is timed separately
     fp8 = None
-    if not args.no_extras and w.d == 128:
+    if not args.no_extras and w.d == 128 and not w.varlen:
         q8, sq = attn.quantize_fp8(q)
         k8, sk = attn.quantize_fp8(k)
         vt8, sv = attn.quantize_fp8(v, transpose=True)
@@ -496,7 +566,7 @@ def run_ours(args, w, rank, world, dist):
     # ---- backward pass on the same shape (non-causal and causal): dQ, dK, dV from the
     # forward's O and LSE and a random upstream gradient
     backward = None
-    if not args.no_extras:
+    if not args.no_extras and not w.varlen:
         backward = {}
         dout = to_dev(w.make_dout())
         bws = torch.empty(max(attn.bwd_workspace_bytes(w.B, w.H, w.N, w.d), 1),
@@ -637,15 +707,17 @@ def run_ours(args, w, rank, world, dist):
             c_gbs = c_bytes / (c_ms * 1e-3) / 1e9
             per_config.append({"workload": cw.name, "ms": c_ms, "tflops": c_tf,
                                "tensor_frac": c_tf / peak, "algorithmic_bytes": c_bytes,
-                               "gbs": c_gbs, "hbm_frac": c_gbs / hbm_peak})
+                               "gbs": c_gbs, "hbm_frac": c_gbs / hbm_peak,
+                               "kernel": kernel_for(cw),
+                               "tensor_pipe_active": profiled_tensor_pipe(cw)})
             del cq, ck, cv, co, cl, cu_d
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, rows, secs = oracle_sample(w, q_np, k_np, v_np, args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"float64 oracle, {rows} query rows (head-major from head (0,0)) "
-                         f"of {w.name}, {secs:.1f} s"}
+        cpu = {"value": tf, "unit": "TFLOPS", **cpu_info(), "kind": "oracle",
+               "sample": f"float64 oracle, {rows} query rows (problem by problem from the "
+                         f"first head) of {w.name}, {secs:.1f} s"}
 
     if rank == 0:
         line = {
@@ -683,8 +755,6 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = configs.WORKLOADS[args.workload]
-    if w.varlen:
-        ap.error("the bench times dense workloads")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None

@@ -26,7 +26,7 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
         if r["kind"] == "fwd":
             tr.write_line(f"fwd {r['case']}: O max {r['o_max_abs']:.2e} mean {r['o_mean_abs']:.2e}"
                           f" over 1e-2 {r['o_over_1e-2']} (|O|<2: {r['o_over_1e-2_below_2']})"
-                          f" ulps<= {r['o_max_ulps_from_rounded']:.0f}"
+                          f" vs rounded {r['o_max_abs_vs_rounded']:.2e}"
                           f" rounded {r['o_frac_correctly_rounded']:.4f}"
                           f" LSE max {r['lse_max_abs']:.2e} n {r['n']}")
         else:
