@@ -142,9 +142,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if ((rc = check_device()) != 0) return rc;
   FwdParams p{};
   const bool varlen = cu_seqlens != nullptr;
-  // dense head dim 128 runs on CTA pairs (one query tile per SM, each SM loading 64-key halves of
-  // the K tiles), split-KV slices included; head dim 64 and packed batches on the two-tile kernel
-  const bool two_sm = d == 128 && !varlen;
+  // head dim 128 runs on CTA pairs (one query tile per SM, each SM loading 64-key halves of the K
+  // tiles), packed batches and split-KV slices included; head dim 64 on the two-tile kernel
+  const bool two_sm = d == 128;
   const uint64_t q_heads = varlen ? static_cast<uint64_t>(H) : static_cast<uint64_t>(B) * H;
   const uint64_t kv_heads = varlen ? static_cast<uint64_t>(Hkv) : static_cast<uint64_t>(B) * Hkv;
   if (encode_rows_map(&p.tm_q, q, d, N, q_heads) != CUDA_SUCCESS ||
@@ -174,7 +174,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if (grid > INT_MAX) return ATTN_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e =
-      two_sm    ? launch_fwd_d128_2sm(p, causal != 0, static_cast<int>(grid), st)
+      two_sm    ? launch_fwd_d128_2sm(p, causal != 0, varlen, static_cast<int>(grid), st)
       : (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, static_cast<int>(grid), st)
                   : launch_fwd_d128(p, causal != 0, varlen, static_cast<int>(grid), st);
   if (e == cudaSuccess && n_splits > 1)

@@ -6,9 +6,9 @@
 namespace attn {
 namespace {
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 cudaError_t launch(const FwdParams& p, int units, cudaStream_t stream) {
-  auto* kernel = attn_fwd_2sm_kernel<CAUSAL>;
+  auto* kernel = attn_fwd_2sm_kernel<CAUSAL, VARLEN>;
   constexpr int kSmem = Fwd2smLayout::kDynBytes;
   // the opt-in for more than 48 KB of dynamic shared memory and the number of clusters that fit
   // at once are per device; remember them (0: not known yet)
@@ -33,7 +33,8 @@ cudaError_t launch(const FwdParams& p, int units, cudaStream_t stream) {
     clusters = n;
     fit[dev & 63].store(clusters, std::memory_order_release);
   }
-  // persistent: one cluster of two CTAs per pair of SMs that fits, each looping over units
+  // persistent: one cluster of two CTAs per pair of SMs that fits, each looping over units (for a
+  // packed batch `units` is an upper bound; the kernel counts the units from cu_seqlens)
   const int grid = 2 * (units < clusters ? units : clusters);
   kernel<<<grid, k2smThreads, kSmem, stream>>>(p);
   return cudaGetLastError();
@@ -41,9 +42,12 @@ cudaError_t launch(const FwdParams& p, int units, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, int units, cudaStream_t stream) {
+cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, bool varlen, int units,
+                                cudaStream_t stream) {
   if (units <= 0) return cudaErrorInvalidValue;
-  return causal ? launch<true>(p, units, stream) : launch<false>(p, units, stream);
+  if (varlen)
+    return causal ? launch<true, true>(p, units, stream) : launch<false, true>(p, units, stream);
+  return causal ? launch<true, false>(p, units, stream) : launch<false, false>(p, units, stream);
 }
 
 }  // namespace attn

@@ -63,6 +63,8 @@ __device__ __forceinline__ void settle(unsigned long long ns) {
 // One work unit: 256 query rows of a head and a slice of their key tiles.
 struct Unit {
   int z;      // head slice of the tensor maps
+  int y0;     // first row of the unit's sequence along the maps' row axis (dense: 0)
+  int len;    // rows of that sequence
   int pt;     // query pair within the sequence
   int split;  // key slice
   int kb;     // first key tile of the slice
@@ -82,6 +84,8 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int u) {
     w.z = L / p.n_qt;
     w.pt = L % p.n_qt;
   }
+  w.y0 = 0;
+  w.len = p.N;
   // key tiles of the row pair (causal: up to the diagonal of its last row); both CTAs run the
   // same count, rank 0's rows of a tile past their diagonal are fully masked
   const int n_keytiles = (p.N + kBN - 1) / kBN;
@@ -92,6 +96,120 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int u) {
   return w;
 }
 
+// ---- packed variable-length batches: where each unit lies
+//
+// Sequence s occupies rows [a_s, a_s + len_s) of every head (cu_seqlens clamped into [0, N]) and
+// has P_s = ceil(len_s / 256) query pairs.  The H * sum_s P_s units (pair, head, sequence) are
+// ordered in bands of kVarBand pair levels, highest band first; inside a band by sequence, then
+// head, then pair level from high to low.  Early bands hold the heavy pairs (causal: more key
+// tiles the higher the level), so the snake walk of next_unit balances the clusters, and the
+// units of one (sequence, head) in a band sit next to each other, so adjacent clusters read the
+// same K and V tiles from L2 at about the same time.
+constexpr int kVarBand = 4;
+
+__device__ __forceinline__ void seq_span(const FwdParams& p, int s, int& a, int& len) {
+  int x = __ldg(p.cu_seqlens + s), y = __ldg(p.cu_seqlens + s + 1);
+  x = min(max(x, 0), p.N);
+  y = min(max(y, x), p.N);
+  a = x;
+  len = y - x;
+}
+
+// Units of sequence s in band b (warp lanes call it for their own s).
+__device__ __forceinline__ int band_units(const FwdParams& p, int s, int b, int& a, int& len) {
+  if (s >= p.B) {
+    a = len = 0;
+    return 0;
+  }
+  seq_span(p, s, a, len);
+  const int pairs = (len + 2 * kBM - 1) / (2 * kBM);
+  return min(max(pairs - kVarBand * b, 0), kVarBand);
+}
+
+__device__ __forceinline__ int warp_sum(int x) {
+  #pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Units of band b over all sequences, times the heads (warp-collective).
+__device__ __forceinline__ int band_count(const FwdParams& p, int b) {
+  const int lane = threadIdx.x & 31;
+  int total = 0;
+  for (int s0 = 0; s0 < p.B; s0 += 32) {
+    int a, len;
+    total += warp_sum(band_units(p, s0 + lane, b, a, len));
+  }
+  return total * p.H;
+}
+
+// Walks the units of one cluster in increasing order (next_unit is increasing in k).  Dense
+// batches need no state; packed batches keep the current band and the sequence chunk reached
+// within it, so each step of the walk costs about one pass over 32 sequences.  Every method is
+// warp-collective for packed batches: all 32 lanes call it with the same u and get the same unit.
+template <bool CAUSAL, bool VARLEN>
+struct Walker {
+  int b = 0;     // current band
+  int cum = 0;   // units before band b
+  int cnt = 0;   // units in band b
+  int cs = 0;    // first sequence of the chunk of 32 reached in band b
+  int ccum = 0;  // units of band b before sequence cs
+
+  __device__ __forceinline__ void init(const FwdParams& p, int max_pairs) {
+    if constexpr (VARLEN) {
+      b = (max_pairs + kVarBand - 1) / kVarBand - 1;
+      cum = cs = ccum = 0;
+      cnt = b >= 0 ? band_count(p, b) : 0;
+    }
+  }
+
+  __device__ __forceinline__ Unit at(const FwdParams& p, int u) {
+    if constexpr (!VARLEN) {
+      return unit_of<CAUSAL>(p, u);
+    } else {
+      const int lane = threadIdx.x & 31;
+      while (u >= cum + cnt && b > 0) {
+        cum += cnt;
+        --b;
+        cnt = band_count(p, b);
+        cs = ccum = 0;
+      }
+      const int i = u - cum;  // index within the band
+      Unit w;
+      w.split = 0;
+      w.kb = 0;
+      for (;;) {
+        int a, len;
+        const int m = band_units(p, cs + lane, b, a, len);
+        const int wgt = m * p.H;
+        int incl = wgt;
+        #pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (i < ccum + total || cs + 32 >= p.B) {
+          const int r = i - ccum;
+          const unsigned hit = __ballot_sync(0xffffffffu, r >= incl - wgt && r < incl);
+          const int src = hit ? __ffs(hit) - 1 : 0;
+          const int r2 = r - __shfl_sync(0xffffffffu, incl - wgt, src);
+          const int ms = max(__shfl_sync(0xffffffffu, m, src), 1);
+          w.y0 = __shfl_sync(0xffffffffu, a, src);
+          w.len = __shfl_sync(0xffffffffu, len, src);
+          w.z = r2 / ms;
+          w.pt = kVarBand * b + ms - 1 - r2 % ms;
+          const int n_keytiles = (w.len + kBN - 1) / kBN;
+          w.n = hit ? (CAUSAL ? min(n_keytiles, 2 * w.pt + 2) : n_keytiles) : 0;
+          return w;
+        }
+        ccum += total;
+        cs += 32;
+      }
+    }
+  }
+};
+
 // The k-th unit of cluster c among G clusters: rounds of G units, taken forward in even rounds
 // and backward in odd ones, so that with units ordered heaviest first every cluster gets a mix.
 __device__ __forceinline__ int next_unit(int k, int c, int G) {
@@ -100,7 +218,7 @@ __device__ __forceinline__ int next_unit(int k, int c, int G) {
 
 }  // namespace fwd2sm
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
     attn_fwd_2sm_kernel(const __grid_constant__ FwdParams p) {
   using Lay = Fwd2smLayout;
@@ -128,10 +246,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_units = p.n_qt * p.B * p.H * p.n_splits;
   const int G = static_cast<int>(gridDim.x) >> 1;  // clusters in the grid
   const int c0 = static_cast<int>(blockIdx.x) >> 1;
-  const int seq_len = p.N;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -158,6 +274,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
     fence_barrier_init();
     misc[1] = 0;
   }
+  if (VARLEN && warp == 2) {
+    // packed batch: the number of units (H * sum of the sequences' query pairs) and the largest
+    // pair count, from cu_seqlens clamped into [0, N]; the first CTA also checks that cu_seqlens
+    // is a prefix sum from 0 to N (a bad one is reported through the status word)
+    int pairs = 0, max_pairs = 0;
+    bool bad = false;
+    for (int s0 = 0; s0 < p.B; s0 += 32) {
+      const int sq = s0 + lane;
+      if (sq < p.B) {
+        int a, len;
+        fwd2sm::seq_span(p, sq, a, len);
+        const int np = (len + 2 * kBM - 1) / (2 * kBM);
+        pairs += np;
+        max_pairs = max(max_pairs, np);
+        if (blockIdx.x == 0) {
+          const int x = __ldg(p.cu_seqlens + sq), y = __ldg(p.cu_seqlens + sq + 1);
+          bad |= (y < x) || (sq == 0 && x != 0) || (sq == p.B - 1 && y != p.N);
+        }
+      }
+    }
+    pairs = fwd2sm::warp_sum(pairs);
+    #pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      max_pairs = max(max_pairs, __shfl_xor_sync(0xffffffffu, max_pairs, off));
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicCAS(p.status, 0, kStatusBadSeqlens);
+    if (lane == 0) {
+      misc[2] = static_cast<uint32_t>(pairs * p.H);
+      misc[3] = static_cast<uint32_t>(max_pairs);
+    }
+  }
   if (warp == 1) {
     tmem_alloc_pair(sbase + Lay::kMisc, 512);
     tmem_relinquish_pair();
@@ -166,37 +312,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
   cluster_sync_all();  // barriers initialised and tensor memory allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  const int n_units = VARLEN ? static_cast<int>(misc[2]) : p.n_qt * p.B * p.H * p.n_splits;
+  const int max_pairs = VARLEN ? static_cast<int>(misc[3]) : 0;
+  // K/V head slice of a query head slice z: query head h reads K/V head h / group; dense maps are
+  // indexed by batch * heads + head, packed maps by head
+  auto kv_slice = [&](int z) {
+    return VARLEN ? z / p.group : (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
+  };
 
   // Counters kept by every role: uq = units with work done so far (selects the Q buffer and the
   // per-unit barrier phases), g = key tiles done so far across units (ring stages, S buffers and
   // their phases).
   if (warp == 0) {
     // ===================================================================== TMA producer
+    // The whole warp walks the units (the packed-batch walk is warp-collective); lane 0 waits and
+    // issues the copies.
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      const uint64_t keep = l2_policy_evict_last();   // K/V are re-read by every query pair
-      const uint64_t once = l2_policy_evict_first();  // Q is read once
-      bool ok = true;
-      int g = 0, uq = 0;
-      for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
-        const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
-        if (w.n == 0) continue;
+    }
+    const uint64_t keep = l2_policy_evict_last();   // K/V are re-read by every query pair
+    const uint64_t once = l2_policy_evict_first();  // Q is read once
+    bool ok = true;
+    int g = 0, uq = 0;
+    fwd2sm::Walker<CAUSAL, VARLEN> walk;
+    walk.init(p, max_pairs);
+    for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
+      const fwd2sm::Unit w = walk.at(p, u);
+      if (w.n == 0) continue;
+      if (lane == 0) {
         const int qb = uq & 1;
-        const int z_kv = (w.z / p.H) * (p.H / p.group) + (w.z % p.H) / p.group;
+        const int z_kv = kv_slice(w.z);
         // the Q buffer was last used by unit uq - 2: its S products have completed
-        if (uq >= 2 && !(ok = mbar_wait(bar(Lay::bQE + qb),
-                                        static_cast<uint32_t>((uq - 2) >> 1) & 1u, wc, 0, 3)))
-          break;
-        if (leader) mbar_arrive_expect_tx(bar(Lay::bQF + qb), 2 * Lay::kQBytes);
-        const int qrow0 = (2 * w.pt + static_cast<int>(rank)) * kBM;
-        #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d_pair(sbase + Lay::kQ + qb * Lay::kQBytes + c * 16384, &p.tm_q,
-                           lbar(Lay::bQF + qb), c * 64, qrow0, w.z, once);
-        for (int j = 0; j < w.n; ++j, ++g) {
+        if (uq >= 2)
+          ok = mbar_wait(bar(Lay::bQE + qb), static_cast<uint32_t>((uq - 2) >> 1) & 1u, wc, 0, 3);
+        if (ok) {
+          if (leader) mbar_arrive_expect_tx(bar(Lay::bQF + qb), 2 * Lay::kQBytes);
+          const int qrow0 = w.y0 + (2 * w.pt + static_cast<int>(rank)) * kBM;
+          #pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d_pair(sbase + Lay::kQ + qb * Lay::kQBytes + c * 16384, &p.tm_q,
+                             lbar(Lay::bQF + qb), c * 64, qrow0, w.z, once);
+        }
+        for (int j = 0; ok && j < w.n; ++j, ++g) {
           const int sk = g % SK, sv = g % SV;
+          const int krow = w.y0 + (w.kb + j) * kBN;
           if (g >= SK &&
               !(ok = mbar_wait(bar(Lay::bKE + sk), (static_cast<uint32_t>(g / SK) & 1u) ^ 1u, wc,
                                0, 1)))
@@ -205,22 +366,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           #pragma unroll
           for (int c = 0; c < 2; ++c)
             tma_load_3d_pair(sbase + Lay::kK + sk * Lay::kKBytes + c * 8192, &p.tm_k,
-                             lbar(Lay::bKF + sk), c * 64,
-                             (w.kb + j) * kBN + 64 * static_cast<int>(rank), z_kv, keep);
+                             lbar(Lay::bKF + sk), c * 64, krow + 64 * static_cast<int>(rank),
+                             z_kv, keep);
           if (g >= SV &&
               !(ok = mbar_wait(bar(Lay::bVE + sv), (static_cast<uint32_t>(g / SV) & 1u) ^ 1u, wc,
                                0, 2)))
             break;
           if (leader) mbar_arrive_expect_tx(bar(Lay::bVF + sv), 2 * Lay::kVBytes);
           tma_load_3d_pair(sbase + Lay::kV + sv * Lay::kVBytes, &p.tm_v, lbar(Lay::bVF + sv),
-                           64 * static_cast<int>(rank), (w.kb + j) * kBN, z_kv, keep);
+                           64 * static_cast<int>(rank), krow, z_kv, keep);
         }
-        ++uq;
       }
-      // unwinding: copies in flight signal rank 0's barriers and land within microseconds;
-      // let them land before the cluster exits
-      if (!ok) fwd2sm::settle(100000ull);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ++uq;
     }
+    // unwinding: copies in flight signal rank 0's barriers and land within microseconds;
+    // let them land before the cluster exits
+    if (!ok && lane == 0) fwd2sm::settle(100000ull);
   } else if (warp == 1 || warp == kSIssuerWarp) {
     // ========================================= MMA issuers (rank 0): P V on warp 1, S on warp 6
     // Two issuing threads, so that each one's waits overlap the other's products: an MMA issue
@@ -234,8 +396,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       if (warp == kSIssuerWarp) {
         constexpr uint32_t kIdS = idesc_bf16_f32(2 * kBM, kBN, false, false);  // Q, K K-major
         const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
+        fwd2sm::Walker<CAUSAL, VARLEN> walk;
+        walk.init(p, max_pairs);
         for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
-          const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
+          const fwd2sm::Unit w = walk.at(p, u);
           if (w.n == 0) continue;
           const int qb = uq & 1;
           const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ + qb * Lay::kQBytes, 16, 1024);
@@ -278,8 +442,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       } else {
         constexpr uint32_t kIdO = idesc_bf16_f32(2 * kBM, D, false, true);  // P (TMEM), V MN
         const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16384, 1024);
+        fwd2sm::Walker<CAUSAL, VARLEN> walk;
+        walk.init(p, max_pairs);
         for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
-          const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
+          const fwd2sm::Unit w = walk.at(p, u);
           if (w.n == 0) continue;
           for (int j = 0; j < w.n; ++j, ++g) {
             const int b = g % NB, sv = g % SV;
@@ -294,6 +460,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
                 !(ok = mbar_wait_warp(bar(Lay::bOE), static_cast<uint32_t>(uq - 1) & 1u, wc,
                                             1, 8)))
               break;
+            if constexpr (VARLEN) {
+              // rows of a sequence's last V tile past its end belong to the next sequence: zero
+              // them in both CTAs' halves (the peer's through the cluster window), so that P = 0
+              // there cannot meet a non-finite value
+              const int valid = w.len - (w.kb + j) * kBN;
+              if (valid < kBN) {
+                const uint32_t vbase = sbase + Lay::kV + sv * Lay::kVBytes;
+                const uint32_t vpeer = mapa_shared(vbase, 1);
+                for (int i = max(valid, 0) * 8 + lane; i < kBN * 8; i += 32) {
+                  st_shared_v4(vbase + i * 16, 0u, 0u, 0u, 0u);
+                  st_shared_cluster_v4(vpeer + i * 16, 0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_cluster();
+              }
+              __syncwarp();
+            }
             tc_fence_after();
             if (lane == 0) {
               const uint64_t bv = desc_v + static_cast<uint64_t>(sv * (Lay::kVBytes >> 4));
@@ -330,14 +512,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
     const size_t plane = static_cast<size_t>(p.n_splits) * rows_total;
     bool ok = true;
     int g = 0, uq = 0;
+    fwd2sm::Walker<CAUSAL, VARLEN> walk;
+    walk.init(p, max_pairs);
     for (int k = 0, u = c0; ok && u < n_units; u = fwd2sm::next_unit(++k, c0, G)) {
-      const fwd2sm::Unit w = fwd2sm::unit_of<CAUSAL>(p, u);
+      const fwd2sm::Unit w = walk.at(p, u);
+      const int seq_len = w.len;
       const int qrow0 = (2 * w.pt + static_cast<int>(rank)) * kBM;  // first row of this tile
       const int row = qrow0 + r;                                     // row within the sequence
       const bool valid = row < seq_len;
       const size_t grow = static_cast<size_t>(w.z) * static_cast<size_t>(p.N) +
-                          static_cast<size_t>(row);
+                          static_cast<size_t>(w.y0) + static_cast<size_t>(row);
       if (w.n == 0) {
+        if (VARLEN) continue;
         // a key slice past the end of this pair's range: the merge reads max -inf and sum 0
         if (valid) {
           const size_t slot = static_cast<size_t>(w.split) * rows_total + grow;
@@ -462,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       if (!(ok = mbar_wait_warp(bar(Lay::bOD), static_cast<uint32_t>(uq) & 1u, wc, 2, 10))) break;
       tc_fence_after();
       const float l_exact = (le[0] + le[1]) + (le[2] + le[3]);
-      if (p.n_splits > 1) {
+      if (!VARLEN && p.n_splits > 1) {
         // this key slice's partial result for the merge: unnormalised O, reference max, row sum
         const size_t slot = static_cast<size_t>(w.split) * rows_total + grow;
         if (valid) {
@@ -521,10 +707,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
         }
         fence_proxy_async_smem();  // the generic-proxy writes above, before the async-proxy reads
         __syncwarp();
-        if (lane == 0 && row0 < seq_len) {
-          tma_store_3d(&p.tm_o, stage, 0, row0, w.z);
-          tma_store_3d(&p.tm_o, stage + 4096, 64, row0, w.z);
-          bulk_commit_group();
+        if (!VARLEN || row0 + 32 <= seq_len) {
+          if (lane == 0 && row0 < seq_len) {
+            tma_store_3d(&p.tm_o, stage, 0, w.y0 + row0, w.z);
+            tma_store_3d(&p.tm_o, stage + 4096, 64, w.y0 + row0, w.z);
+            bulk_commit_group();
+          }
+        } else if (row0 < seq_len) {
+          // the warp's rows run past the end of the sequence, into the next one's rows of the
+          // same tensor: write only the rows of this sequence, 16-byte chunks from the staging
+          // area (lane = chunk of a row, two rows per step)
+          const int nrows = seq_len - row0;
+          __nv_bfloat16* obase = p.o + (static_cast<size_t>(w.z) * static_cast<size_t>(p.N) +
+                                        static_cast<size_t>(w.y0) + static_cast<size_t>(row0)) *
+                                           D;
+          const int cq = lane & 15;  // 16-byte chunk of the row: half cq / 8, chunk cq % 8
+          for (int rr = lane >> 4; rr < nrows; rr += 2) {
+            const uint4 val = *reinterpret_cast<const uint4*>(
+                smem + Lay::kOut + quarter * 8192 + (cq >> 3) * 4096 + rr * 128 +
+                (((cq & 7) ^ (rr & 7)) << 4));
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(rr) * D + cq * 8) = val;
+          }
         }
         if (valid) p.lse[grow] = (m2 + log2f(l_exact)) * 0.69314718055994530942f;
       }

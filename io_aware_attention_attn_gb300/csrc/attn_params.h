@@ -99,7 +99,7 @@ struct Fwd2smLayout {
     bDR = bOE + 1,                 // drain after an abort (leader), one per issuer [2]
     kNumBars = bDR + 2
   };
-  static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort
+  static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2] units [3] pairs
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynBytes = kBytes + 1024;
 };
@@ -112,9 +112,11 @@ cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, bool varlen, int gri
                            cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, bool varlen, int grid,
                             cudaStream_t stream);
-// Dense head dim 128 on CTA pairs, persistent: `units` = query pairs x key slices, spread over as
-// many clusters of two CTAs as fit on the device; p.tm_k has a 64-row box.
-cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, int units, cudaStream_t stream);
+// Head dim 128 on CTA pairs, persistent: `units` = query pairs x key slices (dense) or an upper
+// bound on the query pairs of all sequences times the heads (packed), spread over as many clusters
+// of two CTAs as fit on the device; p.tm_k has a 64-row box, p.tm_o a 32-row box.
+cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, bool varlen, int units,
+                                cudaStream_t stream);
 
 // Split-KV: slices per query pair the library picks when the caller passes num_splits <= 0, and
 // the merge of the slices' partial results (attn_splitkv.cu).  The pick minimises a simple cost

@@ -509,6 +509,20 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// 16-byte store into the shared memory of a CTA of the cluster (`cluster_addr`: window address).
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                                     uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Make this thread's generic-proxy writes to the cluster's shared memory (its own and the peer
+// CTA's) visible to the async proxy (tcgen05 operand reads).
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
 // Arrive on an mbarrier given by its cluster-window address (it may sit in the peer CTA).  The
 // default (CTA-scope release) semantics: the data this arrival publishes lives in tensor memory and
 // is ordered by tcgen05.wait::st and tcgen05.fence::before_thread_sync on the arriving side and

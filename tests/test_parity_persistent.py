@@ -79,3 +79,64 @@ def test_repeated_calls_are_bitwise_equal():
     b = attn.attn_fwd(qd, kd, vd, causal=True, scale=w.scale)
     torch.cuda.synchronize()
     assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16)) and torch.equal(a[1], b[1])
+
+
+# Packed batches on the head-dim-128 kernel: units are (query pair, head, sequence) in bands of
+# pair levels; lengths that are not multiples of 32 leave a softmax warp whose rows run past the
+# end of its sequence (its rows are written one by one instead of by the TMA store), empty and
+# one-row sequences have no units or a single half-empty one.
+PACKED_MANY = [1, 0, 700, 1500, 256, 257, 3000, 0, 129, 1024, 511, 2049]  # 41 pairs per head
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_units_packed(causal):
+    H = 8  # 328 units over the resident clusters: several rounds each
+    q, k, v, cu = configs.custom_varlen(741 + int(causal), PACKED_MANY, H, 128, causal)
+    cu_t = torch.from_numpy(cu).cuda()
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), cu_seqlens=cu_t, causal=causal,
+                           scale=128 ** -0.5)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attention_varlen(q, k, v, cu, causal, 128 ** -0.5)
+    check(to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+          f"packed {'causal' if causal else 'full'} H{H}")
+
+
+def test_many_units_packed_grouped_query():
+    lengths = [33, 900, 0, 1, 2100, 383]
+    q, k, v, cu = configs.custom_varlen(743, lengths, 24, 128, True, H_kv=6)
+    cu_t = torch.from_numpy(cu).cuda()
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), cu_seqlens=cu_t, causal=True,
+                           scale=128 ** -0.5)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attention_gqa_varlen(q, k, v, cu, True, 128 ** -0.5)
+    check(to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, "packed GQA")
+
+
+def test_packed_neighbours_not_read_or_written():
+    # non-finite Q, K and V in the rows of each sequence's neighbours must not reach its output,
+    # and no row of a sequence may be overwritten by the unit of another: the second sequence is
+    # computed from finite inputs and compared in full; the first holds NaN everywhere
+    lengths = [300, 700, 45]
+    q, k, v, cu = configs.custom_varlen(744, lengths, 4, 128, True)
+    q, k, v = q.copy(), k.copy(), v.copy()
+    for x in (q, k, v):
+        x[:, :300] = 0x7FC0
+        x[:, 1000:] = 0x7FC0
+    cu_t = torch.from_numpy(cu).cuda()
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), cu_seqlens=cu_t, causal=True,
+                           scale=128 ** -0.5)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attention_varlen(q[:, 300:1000], k[:, 300:1000], v[:, 300:1000],
+                                          np.array([0, 700], dtype=np.int32), True, 128 ** -0.5)
+    check(to_f64(o)[:, 300:1000], lse.cpu().numpy()[:, 300:1000].astype(np.float64), o_ref,
+          lse_ref, "packed middle sequence between NaN neighbours")
+
+
+def test_packed_repeated_calls_are_bitwise_equal():
+    q, k, v, cu = configs.custom_varlen(745, PACKED_MANY, 4, 128, True)
+    cu_t = torch.from_numpy(cu).cuda()
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    a = attn.attn_fwd(qd, kd, vd, cu_seqlens=cu_t, causal=True)
+    b = attn.attn_fwd(qd, kd, vd, cu_seqlens=cu_t, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16)) and torch.equal(a[1], b[1])

@@ -84,3 +84,88 @@ def test_slice_count_is_within_key_tiles(B, H, N, d):
     assert 1 <= s <= max(1, key_tiles)
     # an explicit request is clamped to the key tiles, never raised
     assert attn.splitkv_slices(B, H, N, d, 3) == min(3, key_tiles)
+
+
+# ---- packed batches: the band walk of the head-dim-128 forward, restated with its warp chunks
+BAND = 4
+
+
+def seq_pairs(cu, N):
+    out = []
+    for s in range(len(cu) - 1):
+        a = min(max(cu[s], 0), N)
+        b = min(max(cu[s + 1], a), N)
+        out.append((a, b - a, (b - a + 2 * BM - 1) // (2 * BM)))
+    return out
+
+
+class PackedWalker:
+    """The kernel's incremental walk: current band, units before it, and the 32-sequence chunk
+    reached within it (a warp handles 32 sequences per step)."""
+
+    def __init__(self, seqs, H):
+        self.seqs, self.H = seqs, H
+        max_pairs = max([p for _, _, p in seqs] + [0])
+        self.b = (max_pairs + BAND - 1) // BAND - 1
+        self.cum, self.cs, self.ccum = 0, 0, 0
+        self.cnt = self.band_count(self.b) if self.b >= 0 else 0
+
+    def band_units(self, s, b):
+        if s >= len(self.seqs):
+            return 0
+        return min(max(self.seqs[s][2] - BAND * b, 0), BAND)
+
+    def band_count(self, b):
+        return self.H * sum(self.band_units(s, b) for s in range(len(self.seqs)))
+
+    def at(self, u):
+        while u >= self.cum + self.cnt and self.b > 0:
+            self.cum += self.cnt
+            self.b -= 1
+            self.cnt = self.band_count(self.b)
+            self.cs = self.ccum = 0
+        i = u - self.cum
+        while True:
+            wgt = [self.H * self.band_units(self.cs + lane, self.b) for lane in range(32)]
+            total = sum(wgt)
+            if i < self.ccum + total or self.cs + 32 >= len(self.seqs):
+                r = i - self.ccum
+                incl = 0
+                for lane in range(32):
+                    if incl <= r < incl + wgt[lane]:
+                        s = self.cs + lane
+                        m = wgt[lane] // self.H
+                        r2 = r - incl
+                        return s, r2 // m, BAND * self.b + m - 1 - r2 % m
+                    incl += wgt[lane]
+                return None
+            self.ccum += total
+            self.cs += 32
+
+
+@pytest.mark.parametrize("lengths,H,G", [
+    ([1, 0, 700, 1500, 256, 257, 3000, 0, 129, 1024, 511, 2049], 8, 76),
+    ([4096] * 3 + [128] * 40 + [0, 1, 2], 3, 76),   # more than 32 sequences: several chunks
+    ([300], 1, 76),
+    ([0, 0, 5], 2, 7),
+    ([257 * k for k in range(70)], 2, 76),
+])
+def test_packed_walk_takes_every_unit_once(lengths, H, G):
+    import numpy as np
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(int).tolist()
+    seqs = seq_pairs(cu, cu[-1])
+    n_units = H * sum(p for _, _, p in seqs)
+    expected = {(s, h, pt) for s, (_, _, p) in enumerate(seqs) for h in range(H)
+                for pt in range(p)}
+    seen = {}
+    for c in range(G):
+        w = PackedWalker(seqs, H)
+        for u in walk(c, G, n_units):
+            unit = w.at(u)
+            assert unit is not None and unit not in seen, (u, unit)
+            seen[unit] = u
+    assert set(seen) == expected
+    # the order is band by band from the top, then sequence, head, and pair level downwards
+    order = sorted(seen, key=lambda x: seen[x])
+    keys = [(-(pt // BAND), s, h, -pt) for s, h, pt in order]
+    assert keys == sorted(keys)
