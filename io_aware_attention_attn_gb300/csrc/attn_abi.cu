@@ -142,15 +142,14 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   if ((rc = check_device()) != 0) return rc;
   FwdParams p{};
   const bool varlen = cu_seqlens != nullptr;
-  // head dim 128 runs on CTA pairs (one query tile per SM, each SM loading 64-key halves of the K
-  // tiles), packed batches and split-KV slices included; head dim 64 on the two-tile kernel
-  const bool two_sm = d == 128;
+  // every forward runs on CTA pairs (one query tile per SM, each SM loading 64-key halves of the K
+  // tiles and writing O in 32-row boxes), packed batches and split-KV slices included
   const uint64_t q_heads = varlen ? static_cast<uint64_t>(H) : static_cast<uint64_t>(B) * H;
   const uint64_t kv_heads = varlen ? static_cast<uint64_t>(Hkv) : static_cast<uint64_t>(B) * Hkv;
   if (encode_rows_map(&p.tm_q, q, d, N, q_heads) != CUDA_SUCCESS ||
-      encode_rows_map(&p.tm_k, k, d, N, kv_heads, two_sm ? 64u : 128u) != CUDA_SUCCESS ||
+      encode_rows_map(&p.tm_k, k, d, N, kv_heads, 64u) != CUDA_SUCCESS ||
       encode_rows_map(&p.tm_v, v, d, N, kv_heads) != CUDA_SUCCESS ||
-      (two_sm && encode_rows_map(&p.tm_o, o, d, N, q_heads, 32u) != CUDA_SUCCESS))
+      encode_rows_map(&p.tm_o, o, d, N, q_heads, 32u) != CUDA_SUCCESS)
     return ATTN_ERR_LAUNCH;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -166,17 +165,14 @@ static int fwd_impl(const void* q, const void* k, const void* v, void* o, float*
   p.part_stat = part_stat;
   p.n_qt = (N + 2 * kBM - 1) / (2 * kBM);  // pairs of 128-row query tiles per head
   p.scale_log2 = scale * 1.4426950408889634f;
-  // work units: (query pair, key slice) per head on the dense kernels, pair slots per head for
-  // packed batches; the two-tile kernel launches one CTA per unit, the two-SM kernel a
-  // persistent grid of clusters over the units
+  // work units: (query pair, key slice) per head for dense batches; for packed batches an upper
+  // bound on the query pairs of all sequences per head (the kernel counts them exactly); a
+  // persistent grid of clusters walks the units
   const long long grid = varlen ? static_cast<long long>(p.n_qt + B) * H
                                  : static_cast<long long>(p.n_qt) * B * H * n_splits;
   if (grid > INT_MAX) return ATTN_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e =
-      two_sm    ? launch_fwd_d128_2sm(p, causal != 0, varlen, static_cast<int>(grid), st)
-      : (d == 64) ? launch_fwd_d64(p, causal != 0, varlen, static_cast<int>(grid), st)
-                  : launch_fwd_d128(p, causal != 0, varlen, static_cast<int>(grid), st);
+  cudaError_t e = launch_fwd_2sm(p, d, causal != 0, varlen, static_cast<int>(grid), st);
   if (e == cudaSuccess && n_splits > 1)
     e = launch_splitkv_combine(d, part_o, part_stat, o, lse, static_cast<long long>(B) * H * N,
                                n_splits, st);

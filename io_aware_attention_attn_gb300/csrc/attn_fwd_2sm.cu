@@ -1,4 +1,4 @@
-// attn_fwd_2sm.cu -- instantiations and launcher of the two-SM fused forward (head dim 128).
+// attn_fwd_2sm.cu -- instantiations and launcher of the two-SM fused forward (head dims 64, 128).
 #include <atomic>
 
 #include "attn_fwd_2sm_kernel.cuh"
@@ -6,10 +6,10 @@
 namespace attn {
 namespace {
 
-template <bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch(const FwdParams& p, int units, cudaStream_t stream) {
-  auto* kernel = attn_fwd_2sm_kernel<CAUSAL, VARLEN>;
-  constexpr int kSmem = Fwd2smLayout::kDynBytes;
+  auto* kernel = attn_fwd_2sm_kernel<D, CAUSAL, VARLEN>;
+  constexpr int kSmem = Fwd2smLayout<D>::kDynBytes;
   // the opt-in for more than 48 KB of dynamic shared memory and the number of clusters that fit
   // at once are per device; remember them (0: not known yet)
   static std::atomic<int> fit[64] = {};
@@ -40,14 +40,23 @@ cudaError_t launch(const FwdParams& p, int units, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_d(const FwdParams& p, bool causal, bool varlen, int units,
+                     cudaStream_t stream) {
+  if (varlen)
+    return causal ? launch<D, true, true>(p, units, stream)
+                  : launch<D, false, true>(p, units, stream);
+  return causal ? launch<D, true, false>(p, units, stream) : launch<D, false, false>(p, units, stream);
+}
+
 }  // namespace
 
-cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, bool varlen, int units,
-                                cudaStream_t stream) {
+cudaError_t launch_fwd_2sm(const FwdParams& p, int d, bool causal, bool varlen, int units,
+                           cudaStream_t stream) {
   if (units <= 0) return cudaErrorInvalidValue;
-  if (varlen)
-    return causal ? launch<true, true>(p, units, stream) : launch<false, true>(p, units, stream);
-  return causal ? launch<true, false>(p, units, stream) : launch<false, false>(p, units, stream);
+  if (d == 64) return launch_d<64>(p, causal, varlen, units, stream);
+  if (d == 128) return launch_d<128>(p, causal, varlen, units, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

@@ -218,14 +218,17 @@ __device__ __forceinline__ int next_unit(int k, int c, int G) {
 
 }  // namespace fwd2sm
 
-template <bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
     attn_fwd_2sm_kernel(const __grid_constant__ FwdParams p) {
-  using Lay = Fwd2smLayout;
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  using Lay = Fwd2smLayout<D>;
   using fwd2sm::f2u;
   using fwd2sm::u2f;
-  constexpr int D = 128;
   constexpr int SK = k2smStagesK, SV = k2smStagesV, NB = k2smSBufs;
+  // P V products are N = 128 wide, 64 value columns from each CTA.  At head dim 64 rank 0 holds
+  // all of V's columns and rank 1's V stages stay zero: O's columns 64..127 are zero and unused.
+  constexpr bool kVBoth = D == 128;
   constexpr uint32_t kColO = 128u * NB;
   constexpr uint16_t kBoth = 0x3;
   constexpr int kSIssuerWarp = 6;
@@ -304,6 +307,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       misc[3] = static_cast<uint32_t>(max_pairs);
     }
   }
+  if (!kVBoth && rank == 1) {
+    // head dim 64: this CTA's half of every V stage is the zero padding of the P V product
+    for (int i = threadIdx.x; i < SV * Lay::kVBytes / 16; i += blockDim.x)
+      st_shared_v4(sbase + Lay::kV + i * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   if (warp == 1) {
     tmem_alloc_pair(sbase + Lay::kMisc, 512);
     tmem_relinquish_pair();
@@ -351,7 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           if (leader) mbar_arrive_expect_tx(bar(Lay::bQF + qb), 2 * Lay::kQBytes);
           const int qrow0 = w.y0 + (2 * w.pt + static_cast<int>(rank)) * kBM;
           #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < D / 64; ++c)
             tma_load_3d_pair(sbase + Lay::kQ + qb * Lay::kQBytes + c * 16384, &p.tm_q,
                              lbar(Lay::bQF + qb), c * 64, qrow0, w.z, once);
         }
@@ -364,15 +373,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
             break;
           if (leader) mbar_arrive_expect_tx(bar(Lay::bKF + sk), 2 * Lay::kKBytes);
           #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < D / 64; ++c)
             tma_load_3d_pair(sbase + Lay::kK + sk * Lay::kKBytes + c * 8192, &p.tm_k,
                              lbar(Lay::bKF + sk), c * 64, krow + 64 * static_cast<int>(rank),
                              z_kv, keep);
+          if (!kVBoth && !leader) continue;  // head dim 64: rank 0 loads all of V's columns
           if (g >= SV &&
               !(ok = mbar_wait(bar(Lay::bVE + sv), (static_cast<uint32_t>(g / SV) & 1u) ^ 1u, wc,
                                0, 2)))
             break;
-          if (leader) mbar_arrive_expect_tx(bar(Lay::bVF + sv), 2 * Lay::kVBytes);
+          if (leader) mbar_arrive_expect_tx(bar(Lay::bVF + sv), (kVBoth ? 2 : 1) * Lay::kVBytes);
           tma_load_3d_pair(sbase + Lay::kV + sv * Lay::kVBytes, &p.tm_v, lbar(Lay::bVF + sv),
                            64 * static_cast<int>(rank), krow, z_kv, keep);
         }
@@ -440,7 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           mbar_wait_drain(bar(Lay::bDR), 0);
         }
       } else {
-        constexpr uint32_t kIdO = idesc_bf16_f32(2 * kBM, D, false, true);  // P (TMEM), V MN
+        constexpr uint32_t kIdO = idesc_bf16_f32(2 * kBM, k2smPVN, false, true);  // P, V MN
         const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16384, 1024);
         fwd2sm::Walker<CAUSAL, VARLEN> walk;
         walk.init(p, max_pairs);
@@ -470,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
                 const uint32_t vpeer = mapa_shared(vbase, 1);
                 for (int i = max(valid, 0) * 8 + lane; i < kBN * 8; i += 32) {
                   st_shared_v4(vbase + i * 16, 0u, 0u, 0u, 0u);
-                  st_shared_cluster_v4(vpeer + i * 16, 0u, 0u, 0u, 0u);
+                  if (kVBoth) st_shared_cluster_v4(vpeer + i * 16, 0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_cluster();
               }
@@ -669,9 +679,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
           }
         }
       } else {
-        // O / l in bf16, staged in this warp's 8 KB area as two 64-column halves of its 32 rows
+        // O / l in bf16, staged in this warp's 8 KB area as D/64 64-column halves of its 32 rows
         // (16-byte chunks XOR-swizzled by row: the tensor map's 128-byte swizzle, and no bank
-        // conflicts), then written by two TMA stores that run on while the warp starts the next
+        // conflicts), then written by D/64 TMA stores that run on while the warp starts the next
         // unit; the map clips rows past the end of the sequence.  The area is rewritten one unit
         // later, once those stores have read it.
         const float inv_l = 1.f / l_exact;
@@ -681,16 +691,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
         uint32_t oa[32], ob[32], oc[32], od[32];
         tmem_ld32(o_col + 0, oa);
         tmem_ld32(o_col + 32, ob);
-        tmem_ld32(o_col + 64, oc);
-        tmem_ld32(o_col + 96, od);
+        if constexpr (D == 128) {
+          tmem_ld32(o_col + 64, oc);
+          tmem_ld32(o_col + 96, od);
+        }
         if (lane == 0) bulk_wait_group_read0();  // the previous unit's stores have read the area
         __syncwarp();
         tmem_wait_ld_regs(oa);
         tmem_wait_ld_regs(ob);
-        tmem_wait_ld_regs(oc);
-        tmem_wait_ld_regs(od);
+        if constexpr (D == 128) {
+          tmem_wait_ld_regs(oc);
+          tmem_wait_ld_regs(od);
+        }
         #pragma unroll
-        for (int hcol = 0; hcol < 2; ++hcol) {
+        for (int hcol = 0; hcol < D / 64; ++hcol) {
           #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const uint32_t* o = hcol == 0 ? (cc == 0 ? oa : ob) : (cc == 0 ? oc : od);
@@ -709,20 +723,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
         __syncwarp();
         if (!VARLEN || row0 + 32 <= seq_len) {
           if (lane == 0 && row0 < seq_len) {
-            tma_store_3d(&p.tm_o, stage, 0, w.y0 + row0, w.z);
-            tma_store_3d(&p.tm_o, stage + 4096, 64, w.y0 + row0, w.z);
+            #pragma unroll
+            for (int hcol = 0; hcol < D / 64; ++hcol)
+              tma_store_3d(&p.tm_o, stage + hcol * 4096, hcol * 64, w.y0 + row0, w.z);
             bulk_commit_group();
           }
         } else if (row0 < seq_len) {
           // the warp's rows run past the end of the sequence, into the next one's rows of the
           // same tensor: write only the rows of this sequence, 16-byte chunks from the staging
-          // area (lane = chunk of a row, two rows per step)
+          // area (lane = chunk of a row; D/8 chunks per row, 256/D rows per step)
+          constexpr int kChunks = D / 8;
           const int nrows = seq_len - row0;
           __nv_bfloat16* obase = p.o + (static_cast<size_t>(w.z) * static_cast<size_t>(p.N) +
                                         static_cast<size_t>(w.y0) + static_cast<size_t>(row0)) *
                                            D;
-          const int cq = lane & 15;  // 16-byte chunk of the row: half cq / 8, chunk cq % 8
-          for (int rr = lane >> 4; rr < nrows; rr += 2) {
+          const int cq = lane % kChunks;  // 16-byte chunk of the row: half cq / 8, chunk cq % 8
+          for (int rr = lane / kChunks; rr < nrows; rr += 32 / kChunks) {
             const uint4 val = *reinterpret_cast<const uint4*>(
                 smem + Lay::kOut + quarter * 8192 + (cq >> 3) * 4096 + rr * 128 +
                 (((cq & 7) ^ (rr & 7)) << 4));

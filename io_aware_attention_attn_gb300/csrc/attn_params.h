@@ -67,17 +67,19 @@ struct PairLayout {
 
 static_assert(PairLayout<128>::kDynBytes <= 232448, "pair kernel exceeds 227 KB shared memory");
 
-// ------------------------------------------- fused kernel, head dim 128: one query tile per SM,
-// two SMs per MMA (a cluster of two CTAs; see attn_fwd_2sm_kernel.cuh)
+// ------------------------------------------------ fused kernel: one query tile per SM, two SMs
+// per MMA (a cluster of two CTAs; see attn_fwd_2sm_kernel.cuh)
 constexpr int k2smThreads = 224;  // 7 warps: producer, P V issuer, 4 softmax, S issuer
 constexpr int k2smStagesK = 4;
 constexpr int k2smStagesV = 4;
 constexpr int k2smSBufs = 3;      // S / P buffers in tensor memory
+constexpr int k2smPVN = 128;      // N of the P V product: D = 128, or D = 64 padded with zero V
+template <int D>
 struct Fwd2smLayout {
-  static constexpr int kQBytes = kBM * 128 * 2;  // this CTA's 128 query rows (two 64-col blocks)
-  static constexpr int kKBytes = 64 * 128 * 2;   // 64 keys of a key tile (two 8 KB blocks)
-  static constexpr int kVBytes = kBN * 64 * 2;   // a key tile's 64 value columns of this CTA
-  static constexpr int kQ = 0;                   // [2]: the current and the next query pair
+  static constexpr int kQBytes = kBM * D * 2;  // this CTA's 128 query rows (D/64 64-col blocks)
+  static constexpr int kKBytes = 64 * D * 2;   // 64 keys of a key tile (D/64 blocks of 8 KB)
+  static constexpr int kVBytes = kBN * 64 * 2; // a key tile's 64 value columns of this CTA
+  static constexpr int kQ = 0;                 // [2]: the current and the next query pair
   static constexpr int kK = kQ + 2 * kQBytes;
   static constexpr int kV = kK + k2smStagesK * kKBytes;
   // epilogue staging [4 warps][2 halves][32 rows x 128 bytes], 1024-byte aligned: the TMA
@@ -102,32 +104,32 @@ struct Fwd2smLayout {
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2] units [3] pairs
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynBytes = kBytes + 1024;
+  static_assert(kOut % 1024 == 0, "O staging must sit on the swizzle atom");
+  static_assert(kDynBytes <= 232448, "two-SM kernel exceeds 227 KB shared memory");
 };
-static_assert(Fwd2smLayout::kOut % 1024 == 0, "O staging must sit on the swizzle atom");
-
-static_assert(Fwd2smLayout::kDynBytes <= 232448, "two-SM kernel exceeds 227 KB shared memory");
 
 // Host launchers (one translation unit per head dimension).
 cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, bool varlen, int grid,
                            cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, bool varlen, int grid,
                             cudaStream_t stream);
-// Head dim 128 on CTA pairs, persistent: `units` = query pairs x key slices (dense) or an upper
-// bound on the query pairs of all sequences times the heads (packed), spread over as many clusters
-// of two CTAs as fit on the device; p.tm_k has a 64-row box, p.tm_o a 32-row box.
-cudaError_t launch_fwd_d128_2sm(const FwdParams& p, bool causal, bool varlen, int units,
-                                cudaStream_t stream);
+// The forward on CTA pairs, persistent (head dim 64 or 128): `units` = query pairs x key slices
+// (dense) or an upper bound on the query pairs of all sequences times the heads (packed), spread
+// over as many clusters of two CTAs as fit on the device; p.tm_k has a 64-row box, p.tm_o a
+// 32-row box.
+cudaError_t launch_fwd_2sm(const FwdParams& p, int d, bool causal, bool varlen, int units,
+                           cudaStream_t stream);
 
 // Split-KV: slices per query pair the library picks when the caller passes num_splits <= 0, and
 // the merge of the slices' partial results (attn_splitkv.cu).  The pick minimises a simple cost
 // model of the launch: waves of (query pair, slice) units times the key tiles one slice visits
 // plus about two tiles of fixed per-unit cost (prologue, epilogue, partial write-out).  A unit is
-// one CTA on one SM at head dim 64 (152 at once) and a cluster of two CTAs on two SMs at head dim
-// 128 (76 at once).
+// a cluster of two CTAs on two SMs (76 at once).
 constexpr int kSmCount = 152;
 constexpr int kMaxSplits = 32;
 inline int splitkv_pick(int B, int H, int N, int d, int num_splits) {
-  const long long slots = d == 128 ? kSmCount / 2 : kSmCount;
+  (void)d;
+  const long long slots = kSmCount / 2;
   const long long pairs = static_cast<long long>((N + 2 * kBM - 1) / (2 * kBM)) * B * H;
   const int key_tiles = (N + kBN - 1) / kBN;
   const int cap = key_tiles < kMaxSplits ? key_tiles : kMaxSplits;
