@@ -44,20 +44,18 @@ METRIC = "fused attention fwd TFLOPS at d=128 N=4096; % of BF16 tensor peak"
 L2_FLUSH_BYTES = 256 << 20
 
 
-# the files that make up each fused forward kernel: a profile taken on other contents is stale
+# the files that make up the fused forward kernel (every bf16 forward runs on it): a profile
+# taken on other contents is stale
 KERNEL_SOURCES = {
     "attn_fwd_2sm_kernel": ("attn_fwd_2sm_kernel.cuh", "attn_params.h", "sm103_ptx.cuh",
                             "attn_fwd_2sm.cu"),
-    "attn_fwd_pair_kernel": ("attn_fwd_pair_kernel.cuh", "attn_params.h", "sm103_ptx.cuh",
-                             "attn_fwd_d64.cu", "attn_fwd_d128.cu"),
 }
 FUSED_SOURCES = KERNEL_SOURCES["attn_fwd_2sm_kernel"]
 
 
 def kernel_for(w) -> str:
-    """The forward kernel the library runs for a workload (dense head dim 128 on CTA pairs;
-    head dim 64 and packed batches on the two-tile kernel)."""
-    return "attn_fwd_2sm_kernel" if (w.d == 128 and not w.varlen) else "attn_fwd_pair_kernel"
+    """The forward kernel the library runs for a workload (CTA pairs for every bf16 forward)."""
+    return "attn_fwd_2sm_kernel"
 
 
 def sources_digest(files=FUSED_SOURCES) -> str:

@@ -210,6 +210,27 @@ struct Walker {
   }
 };
 
+// L2 prefetch of the Q tile and the first two key tiles' K and V halves a CTA loads for unit w
+// (issued while the CTA sets up, so the first loads find them in L2).
+template <int D>
+__device__ __forceinline__ void prefetch_first_tiles(const FwdParams& p, const Unit& w, int z_kv,
+                                                     int rank) {
+  if (w.n == 0) return;
+  // only boxes that start inside the tensor's rows
+  const int qrow = w.y0 + (2 * w.pt + rank) * kBM;
+  #pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    if (qrow < p.N) tma_prefetch_l2_3d(&p.tm_q, c * 64, qrow, w.z);
+    for (int j = 0; j < 2 && j < w.n; ++j) {
+      const int krow = w.y0 + (w.kb + j) * kBN + 64 * rank;
+      if (krow < p.N) tma_prefetch_l2_3d(&p.tm_k, c * 64, krow, z_kv);
+    }
+  }
+  if (D == 128 || rank == 0)
+    for (int j = 0; j < 2 && j < w.n; ++j)
+      tma_prefetch_l2_3d(&p.tm_v, 64 * rank, w.y0 + (w.kb + j) * kBN, z_kv);
+}
+
 // The k-th unit of cluster c among G clusters: rounds of G units, taken forward in even rounds
 // and backward in odd ones, so that with units ordered heaviest first every cluster gets a mix.
 __device__ __forceinline__ int next_unit(int k, int c, int G) {
@@ -252,6 +273,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
   const int G = static_cast<int>(gridDim.x) >> 1;  // clusters in the grid
   const int c0 = static_cast<int>(blockIdx.x) >> 1;
 
+  // K/V head slice of a query head slice z: query head h reads K/V head h / group; dense maps are
+  // indexed by batch * heads + head, packed maps by head
+  auto kv_slice = [&](int z) {
+    return VARLEN ? z / p.group : (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
+  };
+  if (!VARLEN && warp == 0 && lane == 0) {
+    // the tensor maps and this CTA's first tiles start moving while the CTA sets up
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+    if (c0 < p.n_qt * p.B * p.H * p.n_splits) {
+      const fwd2sm::Unit w0 = fwd2sm::unit_of<CAUSAL>(p, c0);
+      fwd2sm::prefetch_first_tiles<D>(p, w0, kv_slice(w0.z), static_cast<int>(rank));
+    }
+  }
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(Lay::bQF + b), 1);
@@ -306,6 +342,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       misc[2] = static_cast<uint32_t>(pairs * p.H);
       misc[3] = static_cast<uint32_t>(max_pairs);
     }
+    if (c0 < pairs * p.H) {
+      // this CTA's first tiles start moving while the CTA sets up
+      fwd2sm::Walker<CAUSAL, VARLEN> walk;
+      walk.init(p, max_pairs);
+      const fwd2sm::Unit w0 = walk.at(p, c0);
+      if (lane == 0) fwd2sm::prefetch_first_tiles<D>(p, w0, kv_slice(w0.z), static_cast<int>(rank));
+    }
   }
   if (!kVBoth && rank == 1) {
     // head dim 64: this CTA's half of every V stage is the zero padding of the P V product
@@ -323,11 +366,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
   const uint32_t tmem = misc[0];
   const int n_units = VARLEN ? static_cast<int>(misc[2]) : p.n_qt * p.B * p.H * p.n_splits;
   const int max_pairs = VARLEN ? static_cast<int>(misc[3]) : 0;
-  // K/V head slice of a query head slice z: query head h reads K/V head h / group; dense maps are
-  // indexed by batch * heads + head, packed maps by head
-  auto kv_slice = [&](int z) {
-    return VARLEN ? z / p.group : (z / p.H) * (p.H / p.group) + (z % p.H) / p.group;
-  };
 
   // Counters kept by every role: uq = units with work done so far (selects the Q buffer and the
   // per-unit barrier phases), g = key tiles done so far across units (ring stages, S buffers and
@@ -753,7 +791,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
       if (lane == 0) mbar_arrive_cluster(lbar(Lay::bOE));
       ++uq;
     }
-    if (lane == 0) bulk_wait_group0();  // this warp's O stores have completed
+    // this warp's O stores have read the staging area (the writes complete with the grid)
+    if (lane == 0) bulk_wait_group_read0();
   }
   tc_fence_before();
   cluster_sync_all();  // no MMA, copy or remote arrival of either CTA is still in flight

@@ -35,38 +35,6 @@ struct FwdParams {
   float scale_log2;          // scale * log2(e)
 };
 
-// ------------------------------------------------------- fused kernel: two query tiles per CTA
-constexpr int kPairThreads = 320;  // 10 warps: producer, MMA, 2 x 4 softmax
-constexpr int kPairStagesK = 2;    // K ring depth
-constexpr int kPairStagesV = 2;    // V ring depth
-
-template <int D>
-struct PairLayout {
-  static constexpr int kTile = kBM * D * 2;  // one 128-row x D bf16 tile (D/64 blocks of 16 KB)
-  static constexpr int kQ = 0;               // Q_0, Q_1
-  static constexpr int kK = kQ + 2 * kTile;
-  static constexpr int kV = kK + kPairStagesK * kTile;
-  static constexpr int kBar = kV + kPairStagesV * kTile;
-  enum {
-    bQ = 0,                      // Q_0 and Q_1 landed
-    bKF = 1,                     // K stage full  [kPairStagesK]
-    bKE = bKF + kPairStagesK,    // K stage free  [kPairStagesK]
-    bVF = bKE + kPairStagesK,    // V stage full  [kPairStagesV]
-    bVE = bVF + kPairStagesV,    // V stage free  [kPairStagesV]
-    bSF = bVE + kPairStagesV,    // S_t written                [2]
-    bPF = bSF + 2,               // P_t written, O_t corrected [2] (128 arrivals)
-    bPV = bPF + 2,               // P_t V_j completed          [2]
-    bOD = bPV + 2,               // last P_t V completed       [2]
-    bDR = bOD + 2,               // drain after an abort
-    kNumBars = bDR + 1
-  };
-  static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..4] tile info
-  static constexpr int kBytes = kMisc + 32;
-  static constexpr int kDynBytes = kBytes + 1024;
-};
-
-static_assert(PairLayout<128>::kDynBytes <= 232448, "pair kernel exceeds 227 KB shared memory");
-
 // ------------------------------------------------ fused kernel: one query tile per SM, two SMs
 // per MMA (a cluster of two CTAs; see attn_fwd_2sm_kernel.cuh)
 constexpr int k2smThreads = 224;  // 7 warps: producer, P V issuer, 4 softmax, S issuer
@@ -108,11 +76,6 @@ struct Fwd2smLayout {
   static_assert(kDynBytes <= 232448, "two-SM kernel exceeds 227 KB shared memory");
 };
 
-// Host launchers (one translation unit per head dimension).
-cudaError_t launch_fwd_d64(const FwdParams& p, bool causal, bool varlen, int grid,
-                           cudaStream_t stream);
-cudaError_t launch_fwd_d128(const FwdParams& p, bool causal, bool varlen, int grid,
-                            cudaStream_t stream);
 // The forward on CTA pairs, persistent (head dim 64 or 128): `units` = query pairs x key slices
 // (dense) or an upper bound on the query pairs of all sequences times the heads (packed), spread
 // over as many clusters of two CTAs as fit on the device; p.tm_k has a 64-row box, p.tm_o a

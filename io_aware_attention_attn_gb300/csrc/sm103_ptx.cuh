@@ -176,6 +176,15 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 3-D tiled prefetch of one box into L2 (no shared memory, no barrier): lets the first tiles a
+// CTA will load travel from HBM while it sets up.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Untiled bulk copy global -> shared of `bytes` bytes (both addresses 16-byte aligned, bytes a
 // multiple of 16), completion signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,

@@ -136,8 +136,9 @@ def test_splitkv_workspace_bytes(lib):
 
 def test_splitkv_slices(lib):
     f = lib.attn_fwd_splitkv_slices
+    # both head dims run on clusters of two SMs (76 at once): the same slice model
     assert f(1, 1, 8192, 128, 0) == 2 and f(1, 2, 8192, 128, 0) == 1
-    assert f(1, 2, 8192, 64, 0) == 2 and f(1, 1, 16384, 64, 0) == 7
+    assert f(1, 2, 8192, 64, 0) == 1 and f(1, 1, 16384, 64, 0) == 7
     assert f(2, 32, 4096, 128, 0) == 1
     assert f(1, 1, 1000, 64, 0) == 8 and f(1, 1, 1000, 64, 3) == 3 and f(1, 1, 1000, 64, 50) == 8
     assert f(1, 1, 1 << 20, 64, 1000) == 32 and f(1, 1, 100, 64, 0) == 1
