@@ -628,9 +628,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2smThreads, 1)
             #pragma unroll
             for (int k = 0; k < 8; ++k) mx[k] = s[k];
             #pragma unroll
-            for (int cc = 8; cc < kBN; cc += 16)
+            for (int cc = 8; cc + 16 <= kBN; cc += 16)  // pairs of 8-key groups: keys 8 .. kBN - 9
               #pragma unroll
               for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[cc + k], s[cc + 8 + k]);
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[kBN - 8 + k]);  // the last 8 keys
             const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
                                    fmaxf(mx[6], mx[7])) * sl2;
             const float m_new = need ? fmaxf(mt, m2) : m2;

@@ -116,11 +116,12 @@ def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, bound: np.ndarray, what: st
 # ------------------------------------------------------------------------------- FP8 path
 # Tolerance of the FP8 forward against exact attention of its dequantized inputs.  The kernel
 # adds the E4M3 rounding of every probability it feeds the P V product (relative error <= 2^-4,
-# half a 3-bit-mantissa spacing) to fp32 accumulation; so |O - O_ref| <= 2^-4 A elementwise with
-# A = sum_k P_k |V_k| / l.  The test allows 2^-3 A on top of the bf16 rounding of O, a mean error
-# of at most 2^-5 mean(A), and the LSE bound of the bf16 path (the scores themselves are exact
-# products of the codes).
-FP8_C = 2.0 ** -3
+# half a 3-bit-mantissa spacing, for normal codes) to fp32 accumulation; so |O - O_ref| <= 2^-4 A
+# elementwise with A = sum_k P_k |V_k| / l.  Codes below 2^-6 (subnormal) carry a larger relative
+# error, so the test allows 1.5 * 2^-4 A on top of the bf16 rounding of O (the largest error
+# measured beyond that rounding is 0.058 A), a mean error of at most 2^-5 mean(A), and the LSE
+# bound of the bf16 path (the scores themselves are exact products of the codes).
+FP8_C = 1.5 * 2.0 ** -4
 FP8_MEAN_C = 2.0 ** -5
 
 
