@@ -71,15 +71,34 @@ struct Unit {
   int n;      // key tiles of the slice (0: nothing to do)
 };
 
+constexpr int kDenseBand = 4;  // pair levels per band of the dense causal order
+
 template <bool CAUSAL>
 __device__ __forceinline__ Unit unit_of(const FwdParams& p, int u) {
   Unit w;
   const int BH = p.B * p.H;
   const int L = u / p.n_splits;
   w.split = u % p.n_splits;
-  if constexpr (CAUSAL) {  // heaviest pairs (most key tiles) first
+  if (CAUSAL && p.n_qt <= 2 * kDenseBand) {
+    // heaviest pairs (most key tiles) first, level by level across the heads (short sequences:
+    // every head's K and V fit in L2 together, and whole levels balance the clusters best)
     w.pt = p.n_qt - 1 - L / BH;
     w.z = L % BH;
+  } else if (CAUSAL) {
+    // heaviest pairs (most key tiles) first, in bands of kDenseBand pair levels from the top;
+    // inside a band all of a head's pairs sit together, so the clusters that take them at about
+    // the same time share that head's K and V tiles in L2
+    const int top = (p.n_qt - 1) / kDenseBand;           // highest band
+    const int m_top = p.n_qt - kDenseBand * top;         // levels in it (the others are full)
+    int b, i, m;
+    if (L < BH * m_top) {
+      b = top, i = L, m = m_top;
+    } else {
+      const int L2 = L - BH * m_top;
+      b = top - 1 - L2 / (BH * kDenseBand), i = L2 % (BH * kDenseBand), m = kDenseBand;
+    }
+    w.z = i / m;
+    w.pt = kDenseBand * b + m - 1 - i % m;
   } else {                 // all pairs of a head together: its K and V stay in L2
     w.z = L / p.n_qt;
     w.pt = L % p.n_qt;

@@ -169,3 +169,29 @@ def test_packed_walk_takes_every_unit_once(lengths, H, G):
     order = sorted(seen, key=lambda x: seen[x])
     keys = [(-(pt // BAND), s, h, -pt) for s, h, pt in order]
     assert keys == sorted(keys)
+
+
+# ---- dense causal batches: bands of four pair levels from the top, a head's pairs together
+DENSE_BAND = 4
+
+
+def dense_causal_unit(L, n_qt, BH):
+    if n_qt <= 2 * DENSE_BAND:  # short sequences: level by level across the heads
+        return L % BH, n_qt - 1 - L // BH
+    top = (n_qt - 1) // DENSE_BAND
+    m_top = n_qt - DENSE_BAND * top
+    if L < BH * m_top:
+        b, i, m = top, L, m_top
+    else:
+        L2 = L - BH * m_top
+        b, i, m = top - 1 - L2 // (BH * DENSE_BAND), L2 % (BH * DENSE_BAND), DENSE_BAND
+    return i // m, DENSE_BAND * b + m - 1 - i % m
+
+
+@pytest.mark.parametrize("n_qt,BH", [(1, 1), (1, 5), (3, 2), (4, 64), (5, 3), (16, 32), (64, 32),
+                                     (9, 7)])
+def test_dense_causal_order_takes_every_pair_once_heaviest_band_first(n_qt, BH):
+    units = [dense_causal_unit(L, n_qt, BH) for L in range(n_qt * BH)]
+    assert sorted(units) == sorted((z, pt) for z in range(BH) for pt in range(n_qt))
+    levels = [pt // (DENSE_BAND if n_qt > 2 * DENSE_BAND else 1) for _, pt in units]
+    assert levels == sorted(levels, reverse=True)
