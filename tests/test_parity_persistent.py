@@ -140,3 +140,21 @@ def test_packed_repeated_calls_are_bitwise_equal():
     b = attn.attn_fwd(qd, kd, vd, cu_seqlens=cu_t, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16)) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, True), (64, False)])
+def test_packed_many_sequences(d, causal):
+    # more sequences than a warp's 32 lanes: the device walk takes the sequences in chunks of 32
+    # within every band; lengths from empty to several pairs
+    rng = np.random.default_rng(761 + d + int(causal))
+    lengths = [int(x) for x in rng.integers(0, 700, size=70)]
+    lengths[3] = 0
+    lengths[40] = 1
+    q, k, v, cu = configs.custom_varlen(761 + d, lengths, 3, d, causal)
+    cu_t = torch.from_numpy(cu).cuda()
+    o, lse = attn.attn_fwd(to_dev(q), to_dev(k), to_dev(v), cu_seqlens=cu_t, causal=causal,
+                           scale=d ** -0.5)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attention_varlen(q, k, v, cu, causal, d ** -0.5)
+    check(to_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref,
+          f"packed 70 sequences d{d} {'causal' if causal else 'full'}")
