@@ -58,10 +58,20 @@ def kernel_for(w) -> str:
     return "attn_fwd_2sm_kernel"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace collapsed (a profile stays valid across
+    comment edits)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def sources_digest(files=FUSED_SOURCES) -> str:
+    """Digest of the kernel's code (comments and whitespace excluded)."""
     h = hashlib.sha256()
     for f in files:
-        h.update(open(os.path.join(ROOT, "io_aware_attention_attn_gb300", "csrc", f), "rb").read())
+        path = os.path.join(ROOT, "io_aware_attention_attn_gb300", "csrc", f)
+        h.update(_code_only(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,23 +1,26 @@
-// attn_fwd_2sm_kernel.cuh -- fused IO-aware attention forward for sm_103a (GB300), head dim 128,
-// one 128-row query tile per SM and one tensor-core product across the two SMs of a TPC.
+// attn_fwd_2sm_kernel.cuh -- fused IO-aware attention forward for sm_103a (GB300), head dim 64
+// or 128, dense or packed batches: one 128-row query tile per SM and one tensor-core product
+// across the two SMs of a TPC.
 //
 // A cluster of two CTAs works on 256 consecutive query rows of one (sequence, head) at a time:
 // the CTA of rank r holds rows 128 r .. 128 r + 127 of them.  Each product is a single
 // cta_group::2 MMA with M = 256 issued by rank 0: S = Q K_j^T takes A (Q) from each CTA's own rows
 // and B (K_j) half from each CTA (keys 64 r .. 64 r + 63 of the tile); O += P V_j takes P from
-// each CTA's tensor memory and V_j's value columns 64 r .. 64 r + 63 from CTA r.  So each SM
-// streams half of every K and V tile (the same K/V bytes per FLOP as two query tiles in one CTA)
-// and holds one query tile, which leaves tensor memory for three S buffers next to O: S_{j+3} can
-// be issued as soon as P_j V_j has completed, while the softmax works on S_{j+1} and S_{j+2}.
-// The tiled loop and online softmax are those of the FlashAttention forward (CS336 Lecture 5
-// notes, section 6.2; the block merge of the CS336 GPU/attention notes, "Online softmax 回顾").
+// each CTA's tensor memory and V_j's value columns 64 r .. 64 r + 63 from CTA r (head dim 64:
+// all 64 columns from rank 0, rank 1's V stages zero).  So each SM streams half of every K and V
+// tile (the same K/V bytes per FLOP as two query tiles in one CTA) and holds one query tile,
+// which leaves tensor memory for three S buffers next to O: S_{j+3} can be issued as soon as
+// P_j V_j has completed, while the softmax works on S_{j+1} and S_{j+2}.  The tiled loop and
+// online softmax are those of the FlashAttention forward (CS336 Lecture 5 notes, section 6.2;
+// the block merge of the CS336 GPU/attention notes, "Online softmax 回顾").
 //
 // The kernel is persistent: the grid holds as many clusters as fit on the GPU at once, and
-// cluster c takes the work units (query pair, key slice) c, 2G - 1 - c, 2G + c, 4G - 1 - c, ...
-// of the non-persistent grid's order (causal: heaviest first), a mix of heavy and light ones.
-// Q is double-buffered, and the K/V rings, the S buffers and every barrier phase run on across
-// units, so the next unit's Q load and first S products overlap the current unit's last tiles
-// and epilogue; only its first P V waits, for the epilogue to have read O.
+// cluster c takes the work units c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... of an order that puts
+// heavy units first (causal and packed batches) and keeps a head's units together where that
+// keeps its K and V in L2 (see unit_of and Walker below).  Q is double-buffered, and the K/V
+// rings, the S buffers and every barrier phase run on across units, so the next unit's Q load
+// and first S products overlap the current unit's last tiles and epilogue; only its first P V
+// waits, for the epilogue to have read O.
 //
 // Warp roles (224 threads per CTA):
 //   warp 0      TMA producer of this CTA's halves: Q per unit, K_j and V_j into four-stage
@@ -31,9 +34,9 @@
 // tile the cluster processes, counted across units, uses buffer g % 3), O at 384.  P (bf16, two
 // per column) overwrites the first 64 columns of its S buffer once the softmax has read it.
 //
-// Softmax in the exp2 domain, with the same sum-triggered reference maximum as the two-tile
-// kernel: a tile is exponentiated against the row's reference m first, and its maximum is taken
-// (m moved, O and l rescaled) only on the first tile or when the tile's row sum exceeds kSumLimit.
+// Softmax in the exp2 domain with a sum-triggered reference maximum: a tile is exponentiated
+// against the row's reference m first, and its maximum is taken (m moved, O and l rescaled) only
+// on the first tile or when the tile's row sum exceeds kSumLimit.
 #pragma once
 
 #include <cuda.h>

@@ -21,6 +21,24 @@ def test_profiled_traffic_follows_the_sources(monkeypatch):
     assert bench.profiled_traffic("no_such_kernel") is None
 
 
+def test_tensor_pipe_lookup_follows_the_sources(monkeypatch):
+    # each workload's committed single-launch summary is found while the kernel's code is the one
+    # it was taken on, and not after any change
+    for i in sorted(configs.WORKLOADS):
+        v = bench.profiled_tensor_pipe(configs.WORKLOADS[i])
+        assert v is None or 0.0 < v <= 100.0
+    monkeypatch.setattr(bench, "sources_digest", lambda files=None: "0" * 16)
+    assert all(bench.profiled_tensor_pipe(configs.WORKLOADS[i]) is None
+               for i in sorted(configs.WORKLOADS))
+
+
+def test_source_digest_ignores_comments_only():
+    a = "int x = 1; // one\n/* block\n comment */ int  y = 2;\n"
+    b = "int x = 1;\nint y = 2; // a different comment\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(a.replace("2", "3"))
+
+
 class _DoneProc:
     def terminate(self):
         pass
