@@ -279,7 +279,9 @@ ATTN_API int attn_fwd_unfused_noalloc(const void* q, const void* k, const void* 
  * after which the kernel drained its in-flight copies, released its tensor memory and returned;
  * bits 8..15 name the waiting role and bits 16..23 the wait site) or 2 (the cu_seqlens given to a
  * packed-batch call was not a non-decreasing prefix sum from 0 to N; the kernel computed on its
- * offsets clamped into [0, N] and read or wrote nothing outside the tensors).  The first problem
+ * offsets clamped into [0, N] and read or wrote nothing outside the tensors) or 3 (a kernel's
+ * shared-memory layout did not fit the dynamic shared memory it was given at a 1024-byte boundary;
+ * that kernel wrote nothing and its outputs are not valid).  The first problem
  * recorded is kept.  Synchronises `stream`, then clears the status.  Returns ATTN_ERR_LAUNCH (< 0)
  * if the status cannot be read.
  */

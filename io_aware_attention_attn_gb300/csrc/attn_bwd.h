@@ -22,8 +22,9 @@
 
 namespace attn {
 
-constexpr int kBwdThreads = 352;  // warp 0 TMA, warps 1 and 10 MMA, warps 2..9 column halves
-constexpr int kBwdStages = 2;     // depth of the streamed-tile rings
+constexpr int kBwdThreads = 352;    // warp 0 TMA, warps 1 and 10 MMA, warps 2..9 column halves
+constexpr int kBwdStages = 2;       // depth of the streamed-tile rings
+constexpr int kBwdStagesQ = 3;      // dK/dV kernel: depth of the Q ring
 
 struct BwdParams {
   CUtensorMap tm_q;   // 3-D maps over [B*H][N][D] bf16, box {64, 128, 1}, 128-byte swizzle
@@ -47,33 +48,40 @@ struct BwdParams {
   float scale;
 };
 
-// dK/dV kernel: K_j and V_j resident; Q_i, dO_i and the per-query vectors (lse2, D) stream
-// through a kBwdStages ring.
+// dK/dV kernel: K_j and V_j resident; Q_i with its -lse2 slice streams through a kBwdStagesQ ring
+// (S^T of query tile t+2 is issued while tile t+1 is being processed, so its Q tile must have
+// landed a tile earlier), dO_i with its -D slice through a kBwdStages ring.  At head dim 128 the
+// tiles take 224 KB; the layout then fits the 227 KB limit only if the dynamic shared memory
+// starts within 312 bytes of a 1024-byte boundary (the kernel checks, and reports
+// kStatusSmemLayout instead of running otherwise).
 template <int D>
 struct BwdKvLayout {
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;                    // [kBwdStages]
-  static constexpr int kDO = kQ + kBwdStages * kTile;      // [kBwdStages]
-  static constexpr int kVec = kDO + kBwdStages * kTile;    // [kBwdStages] x (-lse2[128], -D[128])
-  static constexpr int kBar = kVec + kBwdStages * 1024;
+  static constexpr int kQ = kV + kTile;                    // [kBwdStagesQ]
+  static constexpr int kDO = kQ + kBwdStagesQ * kTile;     // [kBwdStages]
+  static constexpr int kLse = kDO + kBwdStages * kTile;    // [kBwdStagesQ] x -lse2[128]
+  static constexpr int kDvec = kLse + kBwdStagesQ * 512;   // [kBwdStages] x -D[128]
+  static constexpr int kBar = kDvec + kBwdStages * 512;
   enum {
-    bKV = 0,                  // K_j and V_j landed
-    bQF = 1,                  // Q_i, dO_i and vectors landed [kBwdStages]
-    bQE = bQF + kBwdStages,   // stage free (both issuers)    [kBwdStages]
-    bS = bQE + kBwdStages,    // S^T = K Q^T written
-    bDP,                      // dP^T = V dO^T written
-    bP,                       // P^T (bf16) written over S^T (256 arrivals)
-    bDS,                      // dS^T (bf16) written over dP^T (256 arrivals)
-    bDV,                      // dV += P^T dO completed
-    bDK,                      // dK += dS^T Q completed
-    bDR,                      // drain after an abort, one per issuer [2]
+    bKV = 0,                   // K_j and V_j landed
+    bQF = 1,                   // Q_i and its -lse2 landed  [kBwdStagesQ]
+    bQE = bQF + kBwdStagesQ,   // Q stage free              [kBwdStagesQ]
+    bOF = bQE + kBwdStagesQ,   // dO_i and its -D landed    [kBwdStages]
+    bOE = bOF + kBwdStages,    // dO stage free             [kBwdStages]
+    bS = bOE + kBwdStages,     // S^T = K Q^T written               [2 tensor-memory buffers]
+    bSR = bS + 2,              // S^T read by every compute thread (256 arrivals)
+    bDP,                       // dP^T = V dO^T written over the S^T just read
+    bDS,                       // dS^T and P^T (bf16) written over dP^T (256 arrivals)
+    bACC,                      // dV += P^T dO and dK += dS^T Q completed  [2 buffers]
+    bEND = bACC + 2,           // every product of the CTA completed
+    bDR,                       // drain after an abort, one per issuer [2]
     kNumBars = bDR + 2
   };
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..5] tile
   static constexpr int kBytes = kMisc + 32;
-  static constexpr int kDynBytes = kBytes + 1024;
+  static constexpr int kDynBytes = kBytes + 1024 <= 232448 ? kBytes + 1024 : 232448;
 };
 
 // dQ kernel: Q_i and dO_i resident; K_j and V_j stream through rings (K three deep: K_j is

@@ -98,6 +98,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+  if (sbase - raw_s + Lay::kBytes > static_cast<uint32_t>(Lay::kDynBytes)) {
+    // the 1024-byte-aligned layout does not fit what the launch gave (uniform for the CTA)
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kStatusSmemLayout);
+    return;
+  }
   uint8_t* smem = smem_raw + (sbase - raw_s);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);
   const WaitCtx wc{reinterpret_cast<volatile int*>(misc + 1), p.status};
@@ -107,16 +112,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Lay::bKV), 1);
-    for (int s = 0; s < kBwdStages; ++s) {
+    for (int s = 0; s < kBwdStagesQ; ++s) {
       mbar_init(bar(Lay::bQF + s), 1);
-      mbar_init(bar(Lay::bQE + s), 2);  // a commit of each issuer
+      mbar_init(bar(Lay::bQE + s), 1);
+    }
+    for (int s = 0; s < kBwdStages; ++s) {
+      mbar_init(bar(Lay::bOF + s), 1);
+      mbar_init(bar(Lay::bOE + s), 1);
     }
     mbar_init(bar(Lay::bS), 1);
+    mbar_init(bar(Lay::bS + 1), 1);
+    mbar_init(bar(Lay::bSR), 8 * 32);
     mbar_init(bar(Lay::bDP), 1);
-    mbar_init(bar(Lay::bP), 8 * 32);
     mbar_init(bar(Lay::bDS), 8 * 32);
-    mbar_init(bar(Lay::bDV), 1);
-    mbar_init(bar(Lay::bDK), 1);
+    mbar_init(bar(Lay::bACC), 1);
+    mbar_init(bar(Lay::bACC + 1), 1);
+    mbar_init(bar(Lay::bEND), 1);
     mbar_init(bar(Lay::bDR), 1);
     mbar_init(bar(Lay::bDR + 1), 1);
     fence_barrier_init();
@@ -176,7 +187,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  // two 128-column buffers: query tile t uses buffer t & 1 for S^T_t, then (once the compute warps
+  // have loaded S^T_t) for dP^T_t, then for the bf16 P^T_t and dS^T_t the dV and dK products read
+  constexpr uint32_t kColDV = 256, kColDK = 256 + D;
   constexpr uint64_t kTileD = static_cast<uint64_t>(Lay::kTile >> 4);
 
   if (warp == 0) {
@@ -196,78 +209,131 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d_hint(sbase + Lay::kV + c * 16384, &p.tm_v, bar(Lay::bKV), c * 64,
                          y0 + j * kBN, z, once);
       }
-      int issued = 0;
+      int nq = 0, no = 0;
       bool ok = true;
       for (int t = 0; t < n_it; ++t) {
-        const int s = t % kBwdStages;
-        if (t >= kBwdStages &&
-            !(ok = mbar_wait(bar(Lay::bQE + s),
-                             (static_cast<uint32_t>(t / kBwdStages) & 1u) ^ 1u, wc, 0, 1)))
-          break;
+        const int sq = t % kBwdStagesQ, so = t % kBwdStages;
         const int i = i0 + t % n_head;
         const int zq = zq0 + t / n_head;
         const size_t vrow =
             static_cast<size_t>(zq) * p.n_pad + static_cast<size_t>(tbase + i) * kBM;
-        mbar_arrive_expect_tx(bar(Lay::bQF + s), 2 * Lay::kTile + 1024);
+        if (t >= kBwdStagesQ &&
+            !(ok = mbar_wait(bar(Lay::bQE + sq),
+                             (static_cast<uint32_t>(t / kBwdStagesQ) & 1u) ^ 1u, wc, 0, 1)))
+          break;
+        mbar_arrive_expect_tx(bar(Lay::bQF + sq), Lay::kTile + 512);
         #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d_hint(sbase + Lay::kQ + s * Lay::kTile + c * 16384, &p.tm_q,
-                           bar(Lay::bQF + s), c * 64, y0 + i * kBM, zq, keep);
-          tma_load_3d_hint(sbase + Lay::kDO + s * Lay::kTile + c * 16384, &p.tm_do,
-                           bar(Lay::bQF + s), c * 64, y0 + i * kBM, zq, keep);
-        }
-        bulk_load_1d(sbase + Lay::kVec + s * 1024, p.nlse2 + vrow, 512, bar(Lay::bQF + s));
-        bulk_load_1d(sbase + Lay::kVec + s * 1024 + 512, p.nd + vrow, 512, bar(Lay::bQF + s));
-        ++issued;
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sbase + Lay::kQ + sq * Lay::kTile + c * 16384, &p.tm_q,
+                           bar(Lay::bQF + sq), c * 64, y0 + i * kBM, zq, keep);
+        bulk_load_1d(sbase + Lay::kLse + sq * 512, p.nlse2 + vrow, 512, bar(Lay::bQF + sq));
+        ++nq;
+        if (t >= kBwdStages &&
+            !(ok = mbar_wait(bar(Lay::bOE + so),
+                             (static_cast<uint32_t>(t / kBwdStages) & 1u) ^ 1u, wc, 0, 2)))
+          break;
+        mbar_arrive_expect_tx(bar(Lay::bOF + so), Lay::kTile + 512);
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sbase + Lay::kDO + so * Lay::kTile + c * 16384, &p.tm_do,
+                           bar(Lay::bOF + so), c * 64, y0 + i * kBM, zq, keep);
+        bulk_load_1d(sbase + Lay::kDvec + so * 512, p.nd + vrow, 512, bar(Lay::bOF + so));
+        ++no;
       }
       if (!ok) {  // unwinding: let every copy still in flight land before the CTA exits
         mbar_wait_drain(bar(Lay::bKV), 0);
-        for (int t = (issued > kBwdStages ? issued - kBwdStages : 0); t < issued; ++t)
-          mbar_wait_drain(bar(Lay::bQF + t % kBwdStages),
+        for (int t = (nq > kBwdStagesQ ? nq - kBwdStagesQ : 0); t < nq; ++t)
+          mbar_wait_drain(bar(Lay::bQF + t % kBwdStagesQ),
+                          static_cast<uint32_t>(t / kBwdStagesQ) & 1u);
+        for (int t = (no > kBwdStages ? no - kBwdStages : 0); t < no; ++t)
+          mbar_wait_drain(bar(Lay::bOF + t % kBwdStages),
                           static_cast<uint32_t>(t / kBwdStages) & 1u);
       }
     }
   } else if (warp == 1 || warp == 10) {
-    // ============================ MMA issuers: S^T and dV on warp 1, dP^T and dK on warp 10
+    // ============================ MMA issuers: S^T and dP^T on warp 1, dV and dK on warp 10
+    // Query tile t uses buffer t & 1.  Warp 1 issues dP^T_{t+1} once the compute warps have
+    // loaded S^T_{t+1}, then S^T_{t+2} once dV_t and dK_t (which read the buffer) have completed;
+    // warp 10 issues dV_t and dK_t once P^T_t and dS^T_t are written.  An MMA issue blocks until
+    // the tensor pipe accepts it, so with one issuing thread dP^T_{t+1} queued behind all of
+    // dV_t and dK_t; with two it enters the pipe while they are still being issued, and the
+    // compute warps form dS_{t+1} sooner.  P_{t+1} is formed while these products run, and
+    // S^T_{t+2} runs while the compute warps form dS_{t+1}.
     constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
-    const bool chain_s = warp == 1;
-    const uint64_t desc_a = sdesc_sw128(sbase + (chain_s ? Lay::kK : Lay::kV), 16, 1024);
-    const uint64_t desc_b = sdesc_sw128(sbase + (chain_s ? Lay::kQ : Lay::kDO), 16, 1024);
-    // dV reads dO and dK reads Q, both MN-major
-    const uint64_t desc_mn = sdesc_sw128(sbase + (chain_s ? Lay::kDO : Lay::kQ), 16384, 1024);
-    const uint32_t col_ss = chain_s ? kColS : kColDP;
-    const uint32_t col_acc = chain_s ? kColDV : kColDK;
-    const int b_ss = chain_s ? Lay::bS : Lay::bDP;         // SS product written
-    const int b_in = chain_s ? Lay::bP : Lay::bDS;         // its bf16 rewrite by the compute
-    const int b_acc = chain_s ? Lay::bDV : Lay::bDK;       // the TS product completed
+    const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
+    const uint64_t desc_v = sdesc_sw128(sbase + Lay::kV, 16, 1024);
+    const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);         // K-major (S^T)
+    const uint64_t desc_do = sdesc_sw128(sbase + Lay::kDO, 16, 1024);       // K-major (dP^T)
+    const uint64_t desc_q_mn = sdesc_sw128(sbase + Lay::kQ, 16384, 1024);   // MN-major (dK)
+    const uint64_t desc_do_mn = sdesc_sw128(sbase + Lay::kDO, 16384, 1024); // MN-major (dV)
     bool ok = mbar_wait_warp(bar(Lay::bKV), 0, wc, 1, 2);
-    for (int t = 0; ok && t < n_it; ++t) {
-      const int s = t % kBwdStages;
-      const uint32_t par = static_cast<uint32_t>(t) & 1u;
-      if (!(ok = mbar_wait_warp(bar(Lay::bQF + s), static_cast<uint32_t>(t / kBwdStages) & 1u,
-                                wc, 1, 3)))
-        break;
-      // the SS product rewrites the columns the previous TS product read its A operand from
-      if (t > 0 && !(ok = mbar_wait_spin_warp(bar(b_acc), par ^ 1u, wc, 1, chain_s ? 4 : 5)))
-        break;
-      tc_fence_after();
-      if (lane == 0) {
-        bwd::mma_ss_tile<D>(tmem + col_ss, desc_a, desc_b + s * kTileD, kIdSS);
-        mma_commit(bar(b_ss));
+    if (warp == 1) {
+      auto issue_s = [&](int t) -> bool {  // S^T_t = K_j Q_t^T into buffer t & 1
+        const int sq = t % kBwdStagesQ;
+        if (!mbar_wait_warp(bar(Lay::bQF + sq), static_cast<uint32_t>(t / kBwdStagesQ) & 1u, wc,
+                            1, 3))
+          return false;
+        tc_fence_after();
+        if (lane == 0) {
+          bwd::mma_ss_tile<D>(tmem + 128u * static_cast<uint32_t>(t & 1), desc_k,
+                              desc_q + sq * kTileD, kIdSS);
+          mma_commit(bar(Lay::bS + (t & 1)));
+        }
+        __syncwarp();
+        return true;
+      };
+      auto issue_dp = [&](int t) -> bool {  // dP^T_t = V_j dO_t^T over S^T_t, once it is loaded
+        const int so = t % kBwdStages;
+        if (!mbar_wait_warp(bar(Lay::bOF + so), static_cast<uint32_t>(t / kBwdStages) & 1u, wc,
+                            1, 4))
+          return false;
+        if (!mbar_wait_warp(bar(Lay::bSR), static_cast<uint32_t>(t) & 1u, wc, 1, 5)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          bwd::mma_ss_tile<D>(tmem + 128u * static_cast<uint32_t>(t & 1), desc_v,
+                              desc_do + so * kTileD, kIdSS);
+          mma_commit(bar(Lay::bDP));
+        }
+        __syncwarp();
+        return true;
+      };
+      if (ok && n_it > 0) ok = issue_s(0);
+      if (ok && n_it > 1) ok = issue_s(1);
+      if (ok && n_it > 0) ok = issue_dp(0);
+      for (int t = 0; ok && t + 1 < n_it; ++t) {
+        if (!(ok = issue_dp(t + 1))) break;
+        if (t + 2 < n_it) {
+          // buffer t & 1 is free once dV_t and dK_t completed (per-buffer barrier: the next
+          // completion of this one needs dP^T_{t+2}, which this warp issues only after S^T_{t+2})
+          if (!(ok = mbar_wait_warp(bar(Lay::bACC + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u,
+                                    wc, 1, 7)))
+            break;
+          if (!(ok = issue_s(t + 2))) break;
+        }
       }
-      __syncwarp();
-      if (!(ok = mbar_wait_spin_warp(bar(b_in), par, wc, 1, chain_s ? 6 : 7))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        bwd::mma_ts_tile(tmem + col_acc, tmem + col_ss, desc_mn + s * kTileD, kIdTS, t > 0);
-        mma_commit(bar(b_acc));
-        mma_commit(bar(Lay::bQE + s));
+    } else {
+      for (int t = 0; ok && t < n_it; ++t) {
+        const int sq = t % kBwdStagesQ, so = t % kBwdStages;
+        const uint32_t buf = 128u * static_cast<uint32_t>(t & 1);
+        if (!(ok = mbar_wait_warp(bar(Lay::bDS), static_cast<uint32_t>(t) & 1u, wc, 1, 6))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          bwd::mma_ts_tile(tmem + kColDV, tmem + buf + 32, desc_do_mn + so * kTileD, kIdTS, t > 0);
+          bwd::mma_ts_tile(tmem + kColDK, tmem + buf, desc_q_mn + sq * kTileD, kIdTS, t > 0);
+          mma_commit(bar(Lay::bACC + (t & 1)));
+          mma_commit(bar(Lay::bQE + sq));
+          mma_commit(bar(Lay::bOE + so));
+        }
+        __syncwarp();
       }
+      // every product of warp 1 completed before the last dS^T was written, so this commit covers
+      // the CTA's products
+      if (ok && lane == 0) mma_commit(bar(Lay::bEND));
       __syncwarp();
     }
     if (!ok) {  // unwinding: wait for every MMA this thread issued
-      const int dr = Lay::bDR + (chain_s ? 0 : 1);
+      const int dr = Lay::bDR + (warp == 1 ? 0 : 1);
       if (lane == 0) mma_commit(bar(dr));
       __syncwarp();
       mbar_wait_drain(bar(dr), 0);
@@ -278,25 +344,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // key row within the tile (= TMEM lane)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t col_s = t_lane + kColS + 64 * half;
-    const uint32_t col_dp = t_lane + kColDP + 64 * half;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < n_it; ++t) {
-      const int s = t % kBwdStages;
+      const int sq = t % kBwdStagesQ, so = t % kBwdStages;
       const uint32_t par = static_cast<uint32_t>(t) & 1u;
       const int i = i0 + t % n_head;
-      if (!(ok = mbar_wait_warp(bar(Lay::bQF + s), static_cast<uint32_t>(t / kBwdStages) & 1u,
-                                wc, 2, 8)))
+      // this half's 64 query columns of buffer t & 1: S^T, then dP^T, then dS^T (bf16) over the
+      // first 32 columns and P^T (bf16) over the other 32
+      const uint32_t col = t_lane + 128u * static_cast<uint32_t>(t & 1) + 64 * half;
+      if (!(ok = mbar_wait_warp(bar(Lay::bQF + sq), static_cast<uint32_t>(t / kBwdStagesQ) & 1u,
+                                wc, 2, 9)))
         break;
-      if (!(ok = mbar_wait_warp(bar(Lay::bS), par, wc, 2, 9))) break;
+      if (!(ok = mbar_wait_warp(bar(Lay::bS + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 2,
+                                10)))
+        break;
       tc_fence_after();
-      const float* vec = reinterpret_cast<const float*>(smem + Lay::kVec + s * 1024) + 64 * half;
       float pf[64];
       {
         uint32_t u0[32], u1[32];
-        tmem_ld32(col_s, u0);
-        tmem_ld32(col_s + 32, u1);
+        tmem_ld32(col, u0);
+        tmem_ld32(col + 32, u1);
         tmem_wait_ld_regs(u0);
         tmem_wait_ld_regs(u1);
         #pragma unroll
@@ -305,9 +373,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pf[32 + c] = bwd::u2f(u1[c]);
         }
       }
+      tc_fence_before();
+      mbar_arrive(bar(Lay::bSR));  // the buffer may now receive dP^T
+      const float* lvec = reinterpret_cast<const float*>(smem + Lay::kLse + sq * 512) + 64 * half;
       #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {  // P = 2^(s scale log2e - lse2): packed FMAs, then ex2
-        const float4 l = reinterpret_cast<const float4*>(vec)[c4];  // -lse2 of 4 queries
+        const float4 l = reinterpret_cast<const float4*>(lvec)[c4];  // -lse2 of 4 queries
         float x0, x1, x2, x3;
         ffma2(x0, x1, pf[4 * c4], pf[4 * c4 + 1], sl2, sl2, l.x, l.y);
         ffma2(x2, x3, pf[4 * c4 + 2], pf[4 * c4 + 3], sl2, sl2, l.z, l.w);
@@ -320,26 +391,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         #pragma unroll
         for (int c = 0; c < 64; ++c) pf[c] = (64 * half + c < r) ? 0.f : pf[c];
       }
-      {
-        uint32_t pk[32];
-        #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
-        tmem_st32(col_s, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(Lay::bP));
-
-      if (!(ok = mbar_wait_warp(bar(Lay::bDP), par, wc, 2, 10))) break;
+      if (!(ok = mbar_wait_warp(bar(Lay::bOF + so), static_cast<uint32_t>(t / kBwdStages) & 1u,
+                                wc, 2, 11)))
+        break;
+      if (!(ok = mbar_wait_warp(bar(Lay::bDP), par, wc, 2, 12))) break;
       tc_fence_after();
       {
         uint32_t u0[32], u1[32];
-        tmem_ld32(col_dp, u0);
-        tmem_ld32(col_dp + 32, u1);
+        tmem_ld32(col, u0);
+        tmem_ld32(col + 32, u1);
         tmem_wait_ld_regs(u0);
         tmem_wait_ld_regs(u1);
-        const float* dvec = vec + 128;  // -D of this half's 64 queries
-        uint32_t pk[32];
+        const float* dvec =
+            reinterpret_cast<const float*>(smem + Lay::kDvec + so * 512) + 64 * half;  // -D
+        uint32_t pk[32], pp[32];
         #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {  // dS = P (dP - D): packed add and multiply
           const float4 dl = reinterpret_cast<const float4*>(dvec)[c4];
@@ -352,16 +417,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fmul2(d2, d3, pf[4 * c4 + 2], pf[4 * c4 + 3], t2, t3);
           pk[2 * c4] = pack_bf16x2(d0, d1);
           pk[2 * c4 + 1] = pack_bf16x2(d2, d3);
+          pp[2 * c4] = pack_bf16x2(pf[4 * c4], pf[4 * c4 + 1]);
+          pp[2 * c4 + 1] = pack_bf16x2(pf[4 * c4 + 2], pf[4 * c4 + 3]);
         }
-        tmem_st32(col_dp, pk);
+        tmem_st32(col, pk);
+        tmem_st32(col + 32, pp);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(Lay::bDS));
     }
-    // epilogue: the last dK commit covers every MMA of the CTA
-    if (ok) ok = mbar_wait_warp(bar(Lay::bDK), static_cast<uint32_t>(n_it - 1) & 1u, wc, 2, 11);
-    if (ok) ok = mbar_wait_warp(bar(Lay::bDV), static_cast<uint32_t>(n_it - 1) & 1u, wc, 2, 11);
+    // epilogue, once every product of the CTA has completed
+    if (ok) ok = mbar_wait_warp(bar(Lay::bEND), 0, wc, 2, 13);
     if (ok) {
       tc_fence_after();
       const int key = j * kBN + r;
