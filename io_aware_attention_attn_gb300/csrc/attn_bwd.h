@@ -22,7 +22,7 @@
 
 namespace attn {
 
-constexpr int kBwdThreads = 352;    // warp 0 TMA, warps 1 and 10 MMA, warps 2..9 column halves
+constexpr int kBwdThreads = 384;    // warp 0 TMA, warps 1, 10, 11 MMA, warps 2..9 column halves
 constexpr int kBwdStages = 2;       // depth of the streamed-tile rings
 constexpr int kBwdStagesQ = 3;      // dK/dV kernel: depth of the Q ring
 
@@ -52,7 +52,7 @@ struct BwdParams {
 // (S^T of query tile t+2 is issued while tile t+1 is being processed, so its Q tile must have
 // landed a tile earlier), dO_i with its -D slice through a kBwdStages ring.  At head dim 128 the
 // tiles take 224 KB; the layout then fits the 227 KB limit only if the dynamic shared memory
-// starts within 312 bytes of a 1024-byte boundary (the kernel checks, and reports
+// starts within 296 bytes of a 1024-byte boundary (the kernel checks, and reports
 // kStatusSmemLayout instead of running otherwise).
 template <int D>
 struct BwdKvLayout {
@@ -73,11 +73,11 @@ struct BwdKvLayout {
     bS = bOE + kBwdStages,     // S^T = K Q^T written               [2 tensor-memory buffers]
     bSR = bS + 2,              // S^T read by every compute thread (256 arrivals)
     bDP,                       // dP^T = V dO^T written over the S^T just read
-    bDS,                       // dS^T and P^T (bf16) written over dP^T (256 arrivals)
-    bACC,                      // dV += P^T dO and dK += dS^T Q completed  [2 buffers]
+    bDS,                       // dS^T and P^T (bf16) written over dP^T (256 arrivals) [2 buffers]
+    bACC = bDS + 2,            // dV += P^T dO and dK += dS^T Q completed  [2 buffers]
     bEND = bACC + 2,           // every product of the CTA completed
-    bDR,                       // drain after an abort, one per issuer [2]
-    kNumBars = bDR + 2
+    bDR,                       // drain after an abort, one per issuer [3]
+    kNumBars = bDR + 3
   };
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..5] tile
   static constexpr int kBytes = kMisc + 32;
@@ -106,8 +106,8 @@ struct BwdQLayout {
     bDP,                      // dP = dO V^T written            [2 tensor-memory buffers]
     bDS = bDP + 2,            // dS (bf16) written over dP       [2] (256 arrivals)
     bDQ = bDS + 2,            // dQ += dS K from buffer completed [2]
-    bDR = bDQ + 2,            // drain after an abort, one per issuer [2]
-    kNumBars = bDR + 2
+    bDR = bDQ + 2,            // drain after an abort, one per issuer [3]
+    kNumBars = bDR + 3
   };
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base [1] abort [2..5] tile
   static constexpr int kBytes = kMisc + 32;

@@ -4,11 +4,11 @@
 // TMA-fed shared-memory rings, and rebuild P from the saved logsumexp instead of reading any
 // N x N matrix (CS336 Lecture 5 notes, section 6.2, "反向传播怎么办").
 //
-// Warp roles (352 threads): warp 0 TMA producer; warp 1 TMEM owner and an MMA issuer (lane 0);
-// warp 10 the second MMA issuer; warps 2..9 compute.  Each kernel's products form two chains
-// that only meet through the compute warps (dK/dV: S^T -> dV and dP^T -> dK; dQ: S and dP, then
-// dQ), one per issuing thread: an MMA issue blocks until the tensor pipe accepts it, so one
-// thread issuing both chains left the pipe idle during each of its waits.  A compute thread owns one row of the resident tile (its TMEM lane: warp
+// Warp roles (384 threads): warp 0 TMA producer; warp 1 TMEM owner and an MMA issuer (lane 0);
+// warps 10 and 11 MMA issuers; warps 2..9 compute.  Each kernel's products form three streams
+// that only meet through barriers (dK/dV: S^T, dP^T, and dV with dK; dQ: S, dP, dQ), one per
+// issuing thread: an MMA issue blocks until the tensor pipe accepts it, so a thread issuing two
+// streams held the second one back behind every issue and every wait of the first.  A compute thread owns one row of the resident tile (its TMEM lane: warp
 // w may access lanes 32*(w%4)..+31) and one half of the streamed tile's 128 columns: warps 2..5
 // take columns 0..63, warps 6..9 columns 64..127.
 //
@@ -125,11 +125,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(Lay::bSR), 8 * 32);
     mbar_init(bar(Lay::bDP), 1);
     mbar_init(bar(Lay::bDS), 8 * 32);
+    mbar_init(bar(Lay::bDS + 1), 8 * 32);
     mbar_init(bar(Lay::bACC), 1);
     mbar_init(bar(Lay::bACC + 1), 1);
     mbar_init(bar(Lay::bEND), 1);
-    mbar_init(bar(Lay::bDR), 1);
-    mbar_init(bar(Lay::bDR + 1), 1);
+    for (int d = 0; d < 3; ++d) mbar_init(bar(Lay::bDR + d), 1);
     fence_barrier_init();
     misc[1] = 0;
   }
@@ -250,15 +250,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           static_cast<uint32_t>(t / kBwdStages) & 1u);
       }
     }
-  } else if (warp == 1 || warp == 10) {
-    // ============================ MMA issuers: S^T and dP^T on warp 1, dV and dK on warp 10
-    // Query tile t uses buffer t & 1.  Warp 1 issues dP^T_{t+1} once the compute warps have
-    // loaded S^T_{t+1}, then S^T_{t+2} once dV_t and dK_t (which read the buffer) have completed;
-    // warp 10 issues dV_t and dK_t once P^T_t and dS^T_t are written.  An MMA issue blocks until
-    // the tensor pipe accepts it, so with one issuing thread dP^T_{t+1} queued behind all of
-    // dV_t and dK_t; with two it enters the pipe while they are still being issued, and the
-    // compute warps form dS_{t+1} sooner.  P_{t+1} is formed while these products run, and
-    // S^T_{t+2} runs while the compute warps form dS_{t+1}.
+  } else if (warp == 1 || warp == 10 || warp == 11) {
+    // ====================== MMA issuers: S^T on warp 1, dV and dK on warp 10, dP^T on warp 11
+    // Query tile t uses buffer t & 1: S^T_t once dV_{t-2} and dK_{t-2} (which read the buffer)
+    // have completed; dP^T_t over it once the compute warps have loaded S^T_t; dV_t and dK_t once
+    // they have written P^T_t and dS^T_t.  P_{t+1} is formed while dV_t, dK_t and dP^T_{t+1} run,
+    // and S^T_{t+2} runs while the compute warps form dS_{t+1}.
     constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
     const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
@@ -269,11 +266,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t desc_do_mn = sdesc_sw128(sbase + Lay::kDO, 16384, 1024); // MN-major (dV)
     bool ok = mbar_wait_warp(bar(Lay::bKV), 0, wc, 1, 2);
     if (warp == 1) {
-      auto issue_s = [&](int t) -> bool {  // S^T_t = K_j Q_t^T into buffer t & 1
+      for (int t = 0; ok && t < n_it; ++t) {  // S^T_t = K_j Q_t^T into buffer t & 1
         const int sq = t % kBwdStagesQ;
-        if (!mbar_wait_warp(bar(Lay::bQF + sq), static_cast<uint32_t>(t / kBwdStagesQ) & 1u, wc,
-                            1, 3))
-          return false;
+        // the buffer's previous dV and dK products completed (per-buffer barrier: its next
+        // completion needs S^T_t itself)
+        if (t >= 2 && !(ok = mbar_wait_warp(bar(Lay::bACC + (t & 1)),
+                                            static_cast<uint32_t>((t - 2) >> 1) & 1u, wc, 1, 7)))
+          break;
+        if (!(ok = mbar_wait_warp(bar(Lay::bQF + sq), static_cast<uint32_t>(t / kBwdStagesQ) & 1u,
+                                  wc, 1, 3)))
+          break;
         tc_fence_after();
         if (lane == 0) {
           bwd::mma_ss_tile<D>(tmem + 128u * static_cast<uint32_t>(t & 1), desc_k,
@@ -281,14 +283,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(bar(Lay::bS + (t & 1)));
         }
         __syncwarp();
-        return true;
-      };
-      auto issue_dp = [&](int t) -> bool {  // dP^T_t = V_j dO_t^T over S^T_t, once it is loaded
+      }
+    } else if (warp == 11) {
+      for (int t = 0; ok && t < n_it; ++t) {  // dP^T_t = V_j dO_t^T over S^T_t, once it is loaded
         const int so = t % kBwdStages;
-        if (!mbar_wait_warp(bar(Lay::bOF + so), static_cast<uint32_t>(t / kBwdStages) & 1u, wc,
-                            1, 4))
-          return false;
-        if (!mbar_wait_warp(bar(Lay::bSR), static_cast<uint32_t>(t) & 1u, wc, 1, 5)) return false;
+        if (!(ok = mbar_wait_warp(bar(Lay::bOF + so), static_cast<uint32_t>(t / kBwdStages) & 1u,
+                                  wc, 1, 4)))
+          break;
+        if (!(ok = mbar_wait_warp(bar(Lay::bSR), static_cast<uint32_t>(t) & 1u, wc, 1, 5))) break;
         tc_fence_after();
         if (lane == 0) {
           bwd::mma_ss_tile<D>(tmem + 128u * static_cast<uint32_t>(t & 1), desc_v,
@@ -296,27 +298,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(bar(Lay::bDP));
         }
         __syncwarp();
-        return true;
-      };
-      if (ok && n_it > 0) ok = issue_s(0);
-      if (ok && n_it > 1) ok = issue_s(1);
-      if (ok && n_it > 0) ok = issue_dp(0);
-      for (int t = 0; ok && t + 1 < n_it; ++t) {
-        if (!(ok = issue_dp(t + 1))) break;
-        if (t + 2 < n_it) {
-          // buffer t & 1 is free once dV_t and dK_t completed (per-buffer barrier: the next
-          // completion of this one needs dP^T_{t+2}, which this warp issues only after S^T_{t+2})
-          if (!(ok = mbar_wait_warp(bar(Lay::bACC + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u,
-                                    wc, 1, 7)))
-            break;
-          if (!(ok = issue_s(t + 2))) break;
-        }
       }
     } else {
       for (int t = 0; ok && t < n_it; ++t) {
         const int sq = t % kBwdStagesQ, so = t % kBwdStages;
         const uint32_t buf = 128u * static_cast<uint32_t>(t & 1);
-        if (!(ok = mbar_wait_warp(bar(Lay::bDS), static_cast<uint32_t>(t) & 1u, wc, 1, 6))) break;
+        if (!(ok = mbar_wait_warp(bar(Lay::bDS + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 1,
+                                  6)))
+          break;
         tc_fence_after();
         if (lane == 0) {
           bwd::mma_ts_tile(tmem + kColDV, tmem + buf + 32, desc_do_mn + so * kTileD, kIdTS, t > 0);
@@ -327,13 +316,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
       }
-      // every product of warp 1 completed before the last dS^T was written, so this commit covers
-      // the CTA's products
+      // the other issuers' products all completed before the last dS^T was written, so this
+      // commit covers every product of the CTA
       if (ok && lane == 0) mma_commit(bar(Lay::bEND));
       __syncwarp();
     }
     if (!ok) {  // unwinding: wait for every MMA this thread issued
-      const int dr = Lay::bDR + (warp == 1 ? 0 : 1);
+      const int dr = Lay::bDR + (warp == 1 ? 0 : warp == 10 ? 1 : 2);
       if (lane == 0) mma_commit(bar(dr));
       __syncwarp();
       mbar_wait_drain(bar(dr), 0);
@@ -425,7 +414,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(Lay::bDS));
+      mbar_arrive(bar(Lay::bDS + (t & 1)));
     }
     // epilogue, once every product of the CTA has completed
     if (ok) ok = mbar_wait_warp(bar(Lay::bEND), 0, wc, 2, 13);
@@ -480,8 +469,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(Lay::bDS + b), 8 * 32);
       mbar_init(bar(Lay::bDQ + b), 1);
     }
-    mbar_init(bar(Lay::bDR), 1);
-    mbar_init(bar(Lay::bDR + 1), 1);
+    for (int d = 0; d < 3; ++d) mbar_init(bar(Lay::bDR + d), 1);
     fence_barrier_init();
     misc[1] = 0;
   }
@@ -533,7 +521,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = misc[0];
   // S at 0, dQ at 256, dP / dS double-buffered at 128 and 384 (key tile jj uses buffer jj & 1)
   constexpr uint32_t kColS = 0, kColDQ = 256;
-  constexpr uint32_t kColDP[2] = {128, 384};
+  auto dp_col = [](int b) -> uint32_t { return 128u + 256u * static_cast<uint32_t>(b); };
   constexpr uint64_t kTileD = static_cast<uint64_t>(Lay::kTile >> 4);
 
   if (warp == 0) {
@@ -588,8 +576,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           static_cast<uint32_t>(t / kBwdStages) & 1u);
       }
     }
-  } else if (warp == 1 || warp == 10) {
-    // ================================ MMA issuers: S and dP on warp 1, dQ on warp 10
+  } else if (warp == 1 || warp == 10 || warp == 11) {
+    // ======================== MMA issuers: S on warp 1, dQ on warp 10, dP on warp 11
+    // S and dP run ahead of dQ: dP alternates between two tensor-memory buffers, and a buffer is
+    // rewritten once the dQ product that read it (two tiles back) completed; S is rewritten once
+    // every compute thread has read the previous one.
     constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
     const uint64_t desc_q = sdesc_sw128(sbase + Lay::kQ, 16, 1024);
@@ -599,11 +590,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t desc_k_mn = sdesc_sw128(sbase + Lay::kK, 16384, 1024);    // MN-major use
     bool ok = mbar_wait_warp(bar(Lay::bQ), 0, wc, 1, 2);
     if (warp == 1) {
-      // S and dP run ahead of dQ: dP alternates between two tensor-memory buffers, and a buffer
-      // is rewritten once the dQ product that read it (two tiles back) completed; S is rewritten
-      // once every compute thread has read the previous one
-      for (int jj = 0; ok && jj < n_kv; ++jj) {
-        const int sk = jj % kBwdStagesQK, sv = jj % kBwdStages, b = jj & 1;
+      for (int jj = 0; ok && jj < n_kv; ++jj) {  // S = Q_i K_j^T
+        const int sk = jj % kBwdStagesQK;
         if (!(ok = mbar_wait_warp(bar(Lay::bKF + sk),
                                   static_cast<uint32_t>(jj / kBwdStagesQK) & 1u, wc, 1, 3)))
           break;
@@ -617,6 +605,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(bar(Lay::bKE + sk));
         }
         __syncwarp();
+      }
+    } else if (warp == 11) {
+      for (int jj = 0; ok && jj < n_kv; ++jj) {  // dP = dO_i V_j^T into buffer jj & 1
+        const int sv = jj % kBwdStages, b = jj & 1;
         if (!(ok = mbar_wait_warp(bar(Lay::bVF + sv), static_cast<uint32_t>(jj / kBwdStages) & 1u,
                                   wc, 1, 5)))
           break;
@@ -626,21 +618,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         tc_fence_after();
         if (lane == 0) {
-          bwd::mma_ss_tile<D>(tmem + kColDP[b], desc_do, desc_v + sv * kTileD, kIdSS);
+          bwd::mma_ss_tile<D>(tmem + dp_col(b), desc_do, desc_v + sv * kTileD, kIdSS);
           mma_commit(bar(Lay::bDP + b));
           mma_commit(bar(Lay::bVE + sv));
         }
         __syncwarp();
       }
     } else {
-      for (int jj = 0; ok && jj < n_kv; ++jj) {
+      for (int jj = 0; ok && jj < n_kv; ++jj) {  // dQ += dS K_j
         const int sk = jj % kBwdStagesQK, b = jj & 1;
         if (!(ok = mbar_wait_spin_warp(bar(Lay::bDS + b), static_cast<uint32_t>(jj >> 1) & 1u, wc,
                                        1, 7)))
           break;
         tc_fence_after();
         if (lane == 0) {
-          bwd::mma_ts_tile(tmem + kColDQ, tmem + kColDP[b], desc_k_mn + sk * kTileD, kIdTS,
+          bwd::mma_ts_tile(tmem + kColDQ, tmem + dp_col(b), desc_k_mn + sk * kTileD, kIdTS,
                            jj > 0);
           mma_commit(bar(Lay::bDQ + b));
           mma_commit(bar(Lay::bKE + sk));
@@ -649,7 +641,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     if (!ok) {  // unwinding: wait for every MMA this thread issued
-      const int dr = Lay::bDR + (warp == 1 ? 0 : 1);
+      const int dr = Lay::bDR + (warp == 1 ? 0 : warp == 10 ? 1 : 2);
       if (lane == 0) mma_commit(bar(dr));
       __syncwarp();
       mbar_wait_drain(bar(dr), 0);
@@ -701,7 +693,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = 0; c < 64; ++c) pf[c] = (c < lim) ? pf[c] : 0.f;
       }
       const int b = jj & 1;
-      const uint32_t col_dp = t_lane + kColDP[b] + 64 * half;
+      const uint32_t col_dp = t_lane + dp_col(b) + 64 * half;
       if (!(ok = mbar_wait_warp(bar(Lay::bDP + b), static_cast<uint32_t>(jj >> 1) & 1u, wc, 2, 9)))
         break;
       tc_fence_after();
