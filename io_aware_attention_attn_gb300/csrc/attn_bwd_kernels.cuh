@@ -124,8 +124,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(Lay::bS + 1), 1);
     mbar_init(bar(Lay::bSR), 8 * 32);
     mbar_init(bar(Lay::bDP), 1);
-    mbar_init(bar(Lay::bDS), 8 * 32);
-    mbar_init(bar(Lay::bDS + 1), 8 * 32);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(Lay::bP + b), 8 * 32);
+      mbar_init(bar(Lay::bDS + b), 8 * 32);
+    }
     mbar_init(bar(Lay::bACC), 1);
     mbar_init(bar(Lay::bACC + 1), 1);
     mbar_init(bar(Lay::bEND), 1);
@@ -303,12 +305,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int t = 0; ok && t < n_it; ++t) {
         const int sq = t % kBwdStagesQ, so = t % kBwdStages;
         const uint32_t buf = 128u * static_cast<uint32_t>(t & 1);
-        if (!(ok = mbar_wait_warp(bar(Lay::bDS + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 1,
+        // dV_t as soon as P^T_t is written, while the compute warps still form dS_t
+        if (!(ok = mbar_wait_warp(bar(Lay::bP + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 1,
                                   6)))
           break;
         tc_fence_after();
-        if (lane == 0) {
+        if (lane == 0)
           bwd::mma_ts_tile(tmem + kColDV, tmem + buf + 32, desc_do_mn + so * kTileD, kIdTS, t > 0);
+        __syncwarp();
+        if (!(ok = mbar_wait_warp(bar(Lay::bDS + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 1,
+                                  8)))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
           bwd::mma_ts_tile(tmem + kColDK, tmem + buf, desc_q_mn + sq * kTileD, kIdTS, t > 0);
           mma_commit(bar(Lay::bACC + (t & 1)));
           mma_commit(bar(Lay::bQE + sq));
@@ -339,8 +348,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int sq = t % kBwdStagesQ, so = t % kBwdStages;
       const uint32_t par = static_cast<uint32_t>(t) & 1u;
       const int i = i0 + t % n_head;
-      // this half's 64 query columns of buffer t & 1: S^T, then dP^T, then dS^T (bf16) over the
-      // first 32 columns and P^T (bf16) over the other 32
+      // this half's 64 query columns of buffer t & 1: S^T, then dP^T, then P^T (bf16) over the
+      // last 32 columns (written first, for the dV product) and dS^T (bf16) over the first 32
       const uint32_t col = t_lane + 128u * static_cast<uint32_t>(t & 1) + 64 * half;
       if (!(ok = mbar_wait_warp(bar(Lay::bQF + sq), static_cast<uint32_t>(t / kBwdStagesQ) & 1u,
                                 wc, 2, 9)))
@@ -386,31 +395,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!(ok = mbar_wait_warp(bar(Lay::bDP), par, wc, 2, 12))) break;
       tc_fence_after();
       {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(col, u0);
-        tmem_ld32(col + 32, u1);
-        tmem_wait_ld_regs(u0);
-        tmem_wait_ld_regs(u1);
+        // P^T first, over the columns of the second half of dP^T once those are loaded, so the dV
+        // product can start while dS is formed.  dS of queries 32..63 packs into columns that
+        // still hold dP^T of queries 16..31, so it waits in registers until the first half of
+        // dP^T is loaded too.
         const float* dvec =
             reinterpret_cast<const float*>(smem + Lay::kDvec + so * 512) + 64 * half;  // -D
-        uint32_t pk[32], pp[32];
-        #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {  // dS = P (dP - D): packed add and multiply
-          const float4 dl = reinterpret_cast<const float4*>(dvec)[c4];
-          const uint32_t* u = c4 < 8 ? u0 : u1;
-          const int c = 4 * (c4 & 7);
-          float t0, t1, t2, t3, d0, d1, d2, d3;
-          fadd2_to(t0, t1, bwd::u2f(u[c]), bwd::u2f(u[c + 1]), dl.x, dl.y);
-          fadd2_to(t2, t3, bwd::u2f(u[c + 2]), bwd::u2f(u[c + 3]), dl.z, dl.w);
-          fmul2(d0, d1, pf[4 * c4], pf[4 * c4 + 1], t0, t1);
-          fmul2(d2, d3, pf[4 * c4 + 2], pf[4 * c4 + 3], t2, t3);
-          pk[2 * c4] = pack_bf16x2(d0, d1);
-          pk[2 * c4 + 1] = pack_bf16x2(d2, d3);
-          pp[2 * c4] = pack_bf16x2(pf[4 * c4], pf[4 * c4 + 1]);
-          pp[2 * c4 + 1] = pack_bf16x2(pf[4 * c4 + 2], pf[4 * c4 + 3]);
+        auto ds_half = [&](const uint32_t (&u)[32], int h, uint32_t (&pk)[16]) {
+          #pragma unroll
+          for (int q = 0; q < 8; ++q) {  // dS = P (dP - D): packed add and multiply
+            const int c4 = 8 * h + q;
+            const float4 dl = reinterpret_cast<const float4*>(dvec)[c4];
+            float t0, t1, t2, t3, d0, d1, d2, d3;
+            fadd2_to(t0, t1, bwd::u2f(u[4 * q]), bwd::u2f(u[4 * q + 1]), dl.x, dl.y);
+            fadd2_to(t2, t3, bwd::u2f(u[4 * q + 2]), bwd::u2f(u[4 * q + 3]), dl.z, dl.w);
+            fmul2(d0, d1, pf[4 * c4], pf[4 * c4 + 1], t0, t1);
+            fmul2(d2, d3, pf[4 * c4 + 2], pf[4 * c4 + 3], t2, t3);
+            pk[2 * q] = pack_bf16x2(d0, d1);
+            pk[2 * q + 1] = pack_bf16x2(d2, d3);
+          }
+        };
+        uint32_t pk1[16];
+        {
+          uint32_t u1[32];
+          tmem_ld32(col + 32, u1);
+          tmem_wait_ld_regs(u1);
+          uint32_t pp[32];
+          #pragma unroll
+          for (int c = 0; c < 32; ++c) pp[c] = pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
+          tmem_st32(col + 32, pp);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(Lay::bP + (t & 1)));
+          ds_half(u1, 1, pk1);
         }
-        tmem_st32(col, pk);
-        tmem_st32(col + 32, pp);
+        {
+          uint32_t u0[32], pk0[16];
+          tmem_ld32(col, u0);
+          tmem_wait_ld_regs(u0);
+          ds_half(u0, 0, pk0);
+          tmem_st16(col, pk0);
+          tmem_st16(col + 16, pk1);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
