@@ -606,7 +606,7 @@ def run_ours(args, w, rank, world, dist):
                 "ms": b_ms, "tflops": b_flops / (b_ms * 1e-3) / 1e12,
                 "frac_of_peak": b_flops / (b_ms * 1e-3) / 1e12 / peak,
                 "flops_counted": "2.5x forward (5 matmuls); the kernels execute 7",
-                "launches_per_step": 3}
+                "launches_per_step": 2}
             del fo, fl
         backward["workload"] = w.name
         # grouped-query backward on the GQA shape (dK, dV summed over each group of 4)

@@ -3,11 +3,11 @@
 // The backward recomputes S and P tile by tile from the logsumexp the forward saved (CS336
 // Lecture 5 notes, section 6.2, "反向传播怎么办") and applies the chain rule of the definition:
 // dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with D_i = dO_i . O_i, dQ = scale dS K,
-// dK = scale dS^T Q.  Three launches:
+// dK = scale dS^T Q.  Two launches:
 //   bwd_prep_kernel         -D_i and -lse_i * log2(e) per query row, into padded fp32 planes
-//   attn_bwd_dkdv_kernel    one CTA per (head, 128-key tile): dK and dV accumulated in tensor
-//                           memory over the query tiles
-//   attn_bwd_dq_kernel      one CTA per (head, 128-query tile): dQ accumulated in tensor memory
+//   attn_bwd_tiles_kernel   the dK/dV pass, one CTA per (K/V head, 128-key tile): dK and dV
+//                           accumulated in tensor memory over the query tiles; then the dQ pass,
+//                           one CTA per (head, 128-query tile): dQ accumulated in tensor memory
 //                           over the key tiles
 // Every output element is written by exactly one CTA: no atomics, the result is deterministic.
 #pragma once

@@ -23,20 +23,19 @@ cudaError_t allow_smem(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
 
 template <bool CAUSAL, bool VARLEN>
 cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
-  static std::atomic<uint64_t> kv_done{0}, q_done{0};
-  auto* kv = attn_bwd_dkdv_kernel<64, CAUSAL, VARLEN>;
-  auto* qk = attn_bwd_dq_kernel<64, CAUSAL, VARLEN>;
-  constexpr int kKvSmem = BwdKvLayout<64>::kDynBytes;
-  constexpr int kQSmem = BwdQLayout<64>::kDynBytes;
-  cudaError_t e = allow_smem(kv, kKvSmem, kv_done);
-  if (e == cudaSuccess) e = allow_smem(qk, kQSmem, q_done);
+  static std::atomic<uint64_t> done{0};
+  auto* kernel = attn_bwd_tiles_kernel<64, CAUSAL, VARLEN>;
+  constexpr int kSmem = BwdKvLayout<64>::kDynBytes > BwdQLayout<64>::kDynBytes
+                            ? BwdKvLayout<64>::kDynBytes
+                            : BwdQLayout<64>::kDynBytes;
+  cudaError_t e = allow_smem(kernel, kSmem, done);
   if (e != cudaSuccess) return e;
-  // one CTA per (head, 128-row tile); packed batches: per (head, tile slot), past-the-end slots
-  // return at once
-  const int units = VARLEN ? p.n_tiles : p.n_tiles * p.B;
-  kv<<<units * p.H_kv, kBwdThreads, kKvSmem, stream>>>(p);  // per K/V head
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  qk<<<units * p.H, kBwdThreads, kQSmem, stream>>>(p);      // per query head
+  // one CTA per (head, 128-row tile): the dK/dV pass per K/V head, then the dQ pass per query
+  // head; packed batches: per (head, tile slot), past-the-end slots return at once
+  const long long units = VARLEN ? p.n_tiles : static_cast<long long>(p.n_tiles) * p.B;
+  const long long n_kv = units * p.H_kv, n_q = units * p.H;
+  if (n_kv + n_q > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  kernel<<<static_cast<int>(n_kv + n_q), kBwdThreads, kSmem, stream>>>(p, static_cast<int>(n_kv));
   return cudaGetLastError();
 }
 

@@ -91,11 +91,10 @@ __device__ __forceinline__ void store_row_half(uint32_t col, float mul, __nv_bfl
 }  // namespace bwd
 
 // =============================================================================== dK / dV kernel
+// One CTA of the dK/dV pass: key tile slot L (see below).
 template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, uint8_t* smem_raw) {
   using Lay = BwdKvLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t sbase = (raw_s + 1023u) & ~1023u;
   if (sbase - raw_s + Lay::kBytes > static_cast<uint32_t>(Lay::kDynBytes)) {
@@ -140,9 +139,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // that share the K/V head, query tiles j .. n_tiles-1 (causal; the most first) or all of them.
   // dK and dV sum over all of them (grouped-query attention: a shared K/V head's gradient is the
   // sum over its query heads).
-  // Packed batches: z is the K/V head, the tile slot blockIdx.x / H_kv names (sequence, j); rows
-  // are y0 + .. within the packed tensors and the planes' rows of the sequence start at 128 tbase.
-  const int L = static_cast<int>(blockIdx.x);
+  // Packed batches: z is the K/V head, the tile slot L / H_kv names (sequence, j); rows are
+  // y0 + .. within the packed tensors and the planes' rows of the sequence start at 128 tbase.
   int z, j, y0 = 0, seq_len = p.N, tbase = 0;
   if constexpr (!VARLEN) {
     const int BHkv = p.B * p.H_kv;
@@ -464,11 +462,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // =================================================================================== dQ kernel
+// One CTA of the dQ pass: query tile slot L (see below).
 template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, const int L, uint8_t* smem_raw) {
   using Lay = BwdQLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t sbase = (raw_s + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_s);
@@ -501,7 +498,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   // query tile i of head slice z; causal: key tiles 0..i (the heaviest tiles first), else all
-  const int L = static_cast<int>(blockIdx.x);
   int z, i, y0 = 0, seq_len = p.N, tbase = 0;
   if constexpr (!VARLEN) {
     const int BH = p.B * p.H;
@@ -512,7 +508,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       z = L / p.n_tiles;
       i = L % p.n_tiles;
     }
-  } else {  // packed batches: z is the head, the slot blockIdx.x / H names (sequence, i)
+  } else {  // packed batches: z is the head, the slot L / H names (sequence, i)
     z = L % p.H;
     if (warp == 0) {
       int start, len, tile, base;
@@ -763,6 +759,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Both passes in one launch: CTAs 0 .. n_kv_ctas-1 run the dK/dV pass, the others the dQ pass.
+// CTAs start roughly in index order, so the dQ pass fills the SMs the dK/dV pass leaves idle in
+// its last, partial wave (two launches each ended in one).
+template <int D, bool CAUSAL, bool VARLEN>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_tiles_kernel(const __grid_constant__ BwdParams p, int n_kv_ctas) {
+  extern __shared__ uint8_t smem_raw[];
+  const int L = static_cast<int>(blockIdx.x);
+  if (L < n_kv_ctas)
+    bwd_dkdv_cta<D, CAUSAL, VARLEN>(p, L, smem_raw);
+  else
+    bwd_dq_cta<D, CAUSAL, VARLEN>(p, L - n_kv_ctas, smem_raw);
 }
 
 }  // namespace attn

@@ -13,6 +13,34 @@
 namespace attn {
 namespace {
 
+// One row of O and of dO is D/8 chunks of 16 bytes.  prep_dot is a lane's share of dO . O over
+// its chunk; prep_reduce sums the shares of the D/8 lanes that hold one row.  Both passes below
+// use them, in the same order, so a packed batch of one sequence reproduces the dense planes bit
+// for bit.
+template <int D>
+__device__ __forceinline__ float prep_dot(const uint4& a, const uint4& b) {
+  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float acc = 0.f;
+  #pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 x = __bfloat1622float2(a2[q]), y = __bfloat1622float2(b2[q]);
+    acc = fmaf(x.x, y.x, acc);
+    acc = fmaf(x.y, y.y, acc);
+  }
+  return acc;
+}
+template <int D>
+__device__ __forceinline__ float prep_reduce(float acc) {
+  #pragma unroll
+  for (int sft = D / 16; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+  return acc;
+}
+
+// Dense batches: each warp takes 8 consecutive plane rows (never across heads: n_pad is a
+// multiple of 128).  A row of O and of dO is D/8 chunks of 16 bytes, one per lane, so a warp's
+// load instruction covers 32 / (D/8) rows and every lane has 8 / (32 / (D/8)) loads of each
+// tensor in flight before it reduces.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout,
@@ -20,42 +48,42 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        float* __restrict__ nlse2,
                                                        float* __restrict__ nd, long long rows_pad,
                                                        int N, int n_pad) {
-  constexpr int kPer = D / 32;  // elements per lane
-  const long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (w >= rows_pad) return;
+  constexpr int kLanes = D / 8;          // 16-byte chunks per row
+  constexpr int kRowsPer = 32 / kLanes;  // rows per warp-wide load
+  constexpr int kIters = 8 / kRowsPer;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * 8;
+  if (w0 >= rows_pad) return;
   const int lane = threadIdx.x & 31;
-  const long long z = w / n_pad;
-  const int row = static_cast<int>(w % n_pad);
-  if (row >= N) {
-    if (lane == 0) {
-      nlse2[w] = -INFINITY;
-      nd[w] = 0.f;
+  const int sub = lane / kLanes, chunk = lane % kLanes;
+  uint4 a[kIters], b[kIters];
+  #pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const long long w = w0 + it * kRowsPer + sub;
+    const long long z = w / n_pad;
+    const int row = static_cast<int>(w % n_pad);
+    a[it] = make_uint4(0u, 0u, 0u, 0u);
+    b[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (w < rows_pad && row < N) {
+      const size_t off = (static_cast<size_t>(z) * N + row) * D + chunk * 8;
+      a[it] = __ldg(reinterpret_cast<const uint4*>(o + off));
+      b[it] = __ldg(reinterpret_cast<const uint4*>(dout + off));
     }
-    return;
-  }
-  const size_t off = (static_cast<size_t>(z) * N + row) * D + lane * kPer;
-  float acc = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-    #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const float2 x = __bfloat1622float2(a2[q]), y = __bfloat1622float2(b2[q]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
-    }
-  } else {
-    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + off));
-    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + off));
-    acc = fmaf(x.x, y.x, x.y * y.y);
   }
   #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    nd[w] = -acc;
-    nlse2[w] = -lse[static_cast<size_t>(z) * N + row] * 1.4426950408889634f;
+  for (int it = 0; it < kIters; ++it) {
+    const float acc = prep_reduce<D>(prep_dot<D>(a[it], b[it]));
+    const long long w = w0 + it * kRowsPer + sub;
+    if (chunk == 0 && w < rows_pad) {
+      const long long z = w / n_pad;
+      const int row = static_cast<int>(w % n_pad);
+      if (row < N) {
+        nd[w] = -acc;
+        nlse2[w] = -lse[static_cast<size_t>(z) * N + row] * 1.4426950408889634f;
+      } else {
+        nlse2[w] = -INFINITY;
+        nd[w] = 0.f;
+      }
+    }
   }
 }
 
@@ -66,7 +94,6 @@ __global__ void __launch_bounds__(256) bwd_prep_varlen_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
     const float* __restrict__ lse, float* __restrict__ nlse2, float* __restrict__ nd,
     const int32_t* __restrict__ cu, int n_seqs, int H, int T, int n_slots) {
-  constexpr int kPer = D / 32;
   __shared__ int info[3];
   const int z = blockIdx.x % H, slot = blockIdx.x / H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -84,39 +111,28 @@ __global__ void __launch_bounds__(256) bwd_prep_varlen_kernel(
   if (tile < 0) return;  // past the last tile: these plane rows are never read
   const size_t prow = static_cast<size_t>(z) * (static_cast<size_t>(n_slots) * kBM) +
                       static_cast<size_t>(slot) * kBM;
-  for (int r = warp * 16; r < warp * 16 + 16; ++r) {
+  // each warp takes 16 rows of the tile, 32 / (D/8) rows per load as in the dense pass
+  constexpr int kLanes = D / 8, kRowsPer = 32 / kLanes;
+  const int sub = lane / kLanes, chunk = lane % kLanes;
+  for (int r0 = warp * 16; r0 < warp * 16 + 16; r0 += kRowsPer) {
+    const int r = r0 + sub;
     const int in_seq = tile * kBM + r;
-    if (in_seq >= len) {
-      if (lane == 0) {
+    const bool valid = in_seq < len;
+    const size_t row = static_cast<size_t>(z) * T + start + (valid ? in_seq : 0);
+    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      a = __ldg(reinterpret_cast<const uint4*>(o + row * D + chunk * 8));
+      b = __ldg(reinterpret_cast<const uint4*>(dout + row * D + chunk * 8));
+    }
+    const float acc = prep_reduce<D>(prep_dot<D>(a, b));
+    if (chunk == 0) {
+      if (valid) {
+        nd[prow + r] = -acc;
+        nlse2[prow + r] = -lse[row] * 1.4426950408889634f;
+      } else {
         nlse2[prow + r] = -INFINITY;
         nd[prow + r] = 0.f;
       }
-      continue;
-    }
-    const size_t row = static_cast<size_t>(z) * T + start + in_seq;
-    const size_t off = row * D + lane * kPer;
-    float acc = 0.f;
-    if constexpr (kPer == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-      const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-      #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float2 x = __bfloat1622float2(a2[q]), y = __bfloat1622float2(b2[q]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-    } else {
-      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + off));
-      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + off));
-      acc = fmaf(x.x, y.x, x.y * y.y);
-    }
-    #pragma unroll
-    for (int sft = 16; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
-    if (lane == 0) {
-      nd[prow + r] = -acc;
-      nlse2[prow + r] = -lse[row] * 1.4426950408889634f;
     }
   }
 }
@@ -142,7 +158,7 @@ cudaError_t launch_bwd_prep_varlen(const void* o, const void* dout, const float*
 cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* nlse2,
                             float* nd, int BH, int N, int n_pad, int d, cudaStream_t stream) {
   const long long rows_pad = static_cast<long long>(BH) * n_pad;
-  const long long blocks = (rows_pad + 7) / 8;
+  const long long blocks = (rows_pad + 63) / 64;  // 8 warps of 8 rows
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const auto* ob = static_cast<const __nv_bfloat16*>(o);
   const auto* db = static_cast<const __nv_bfloat16*>(dout);
