@@ -76,7 +76,7 @@ struct BwdKvLayout {
     bP,                        // P^T (bf16) written over dP^T (256 arrivals)  [2 buffers]
     bDS = bP + 2,              // dS^T (bf16) written over dP^T (256 arrivals) [2 buffers]
     bACC = bDS + 2,            // dV += P^T dO and dK += dS^T Q completed  [2 buffers]
-    bEND = bACC + 2,           // every product of the CTA completed
+    bEND = bACC + 2,           // every product of the CTA completed (dV and dK issuers)
     bDR,                       // drain after an abort, one per issuer [3]
     kNumBars = bDR + 3
   };

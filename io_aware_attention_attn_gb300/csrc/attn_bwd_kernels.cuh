@@ -127,9 +127,9 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
       mbar_init(bar(Lay::bP + b), 8 * 32);
       mbar_init(bar(Lay::bDS + b), 8 * 32);
     }
-    mbar_init(bar(Lay::bACC), 1);
-    mbar_init(bar(Lay::bACC + 1), 1);
-    mbar_init(bar(Lay::bEND), 1);
+    mbar_init(bar(Lay::bACC), 2);      // a commit of each of the dV and dK issuers
+    mbar_init(bar(Lay::bACC + 1), 2);
+    mbar_init(bar(Lay::bEND), 2);
     for (int d = 0; d < 3; ++d) mbar_init(bar(Lay::bDR + d), 1);
     fence_barrier_init();
     misc[1] = 0;
@@ -251,11 +251,14 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
       }
     }
   } else if (warp == 1 || warp == 10 || warp == 11) {
-    // ====================== MMA issuers: S^T on warp 1, dV and dK on warp 10, dP^T on warp 11
+    // ====================== MMA issuers: S^T and dK on warp 1, dV on warp 10, dP^T on warp 11
     // Query tile t uses buffer t & 1: S^T_t once dV_{t-2} and dK_{t-2} (which read the buffer)
-    // have completed; dP^T_t over it once the compute warps have loaded S^T_t; dV_t and dK_t once
-    // they have written P^T_t and dS^T_t.  P_{t+1} is formed while dV_t, dK_t and dP^T_{t+1} run,
-    // and S^T_{t+2} runs while the compute warps form dS_{t+1}.
+    // have completed; dP^T_t over it once the compute warps have loaded S^T_t; dV_t once they
+    // have written P^T_t, dK_t once they have written dS^T_t.  P_{t+1} is formed while dV_t and
+    // dP^T_{t+1} run, and S^T_{t+2} runs while the compute warps form dS_{t+1}.  dK_t and S^T_{t+2}
+    // sit on the critical path (dS_t written -> dK_t -> S^T_{t+2} -> the compute warps), so they
+    // share a warp that is idle when dS_t is written; an MMA issue blocks until the tensor pipe
+    // accepts it, and the dV issuer is then often still blocked in dV_t.
     constexpr uint32_t kIdSS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t kIdTS = idesc_bf16_f32(kBM, D, false, true);
     const uint64_t desc_k = sdesc_sw128(sbase + Lay::kK, 16, 1024);
@@ -266,16 +269,11 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
     const uint64_t desc_do_mn = sdesc_sw128(sbase + Lay::kDO, 16384, 1024); // MN-major (dV)
     bool ok = mbar_wait_warp(bar(Lay::bKV), 0, wc, 1, 2);
     if (warp == 1) {
-      for (int t = 0; ok && t < n_it; ++t) {  // S^T_t = K_j Q_t^T into buffer t & 1
+      auto issue_s = [&](int t) -> bool {  // S^T_t = K_j Q_t^T into buffer t & 1
         const int sq = t % kBwdStagesQ;
-        // the buffer's previous dV and dK products completed (per-buffer barrier: its next
-        // completion needs S^T_t itself)
-        if (t >= 2 && !(ok = mbar_wait_warp(bar(Lay::bACC + (t & 1)),
-                                            static_cast<uint32_t>((t - 2) >> 1) & 1u, wc, 1, 7)))
-          break;
-        if (!(ok = mbar_wait_warp(bar(Lay::bQF + sq), static_cast<uint32_t>(t / kBwdStagesQ) & 1u,
-                                  wc, 1, 3)))
-          break;
+        if (!mbar_wait_warp(bar(Lay::bQF + sq), static_cast<uint32_t>(t / kBwdStagesQ) & 1u, wc,
+                            1, 3))
+          return false;
         tc_fence_after();
         if (lane == 0) {
           bwd::mma_ss_tile<D>(tmem + 128u * static_cast<uint32_t>(t & 1), desc_k,
@@ -283,6 +281,31 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
           mma_commit(bar(Lay::bS + (t & 1)));
         }
         __syncwarp();
+        return true;
+      };
+      if (ok && n_it > 0) ok = issue_s(0);
+      if (ok && n_it > 1) ok = issue_s(1);
+      for (int t = 0; ok && t < n_it; ++t) {
+        const int sq = t % kBwdStagesQ;
+        const uint32_t buf = 128u * static_cast<uint32_t>(t & 1);
+        if (!(ok = mbar_wait_warp(bar(Lay::bDS + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 1,
+                                  8)))
+          break;
+        tc_fence_after();
+        if (lane == 0) {  // dK_t += dS^T_t Q_t
+          bwd::mma_ts_tile(tmem + kColDK, tmem + buf, desc_q_mn + sq * kTileD, kIdTS, t > 0);
+          mma_commit(bar(Lay::bACC + (t & 1)));
+          mma_commit(bar(Lay::bQE + sq));
+        }
+        __syncwarp();
+        if (t + 2 < n_it) {
+          // the buffer is free once dV_t and dK_t completed (per-buffer barrier: its next
+          // completion needs dK_{t+2}, which this warp issues after S^T_{t+2})
+          if (!(ok = mbar_wait_warp(bar(Lay::bACC + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u,
+                                    wc, 1, 7)))
+            break;
+          if (!(ok = issue_s(t + 2))) break;
+        }
       }
     } else if (warp == 11) {
       for (int t = 0; ok && t < n_it; ++t) {  // dP^T_t = V_j dO_t^T over S^T_t, once it is loaded
@@ -300,32 +323,25 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
         __syncwarp();
       }
     } else {
-      for (int t = 0; ok && t < n_it; ++t) {
-        const int sq = t % kBwdStagesQ, so = t % kBwdStages;
+      for (int t = 0; ok && t < n_it; ++t) {  // dV_t += P^T_t dO_t
+        const int so = t % kBwdStages;
         const uint32_t buf = 128u * static_cast<uint32_t>(t & 1);
-        // dV_t as soon as P^T_t is written, while the compute warps still form dS_t
         if (!(ok = mbar_wait_warp(bar(Lay::bP + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 1,
                                   6)))
           break;
         tc_fence_after();
-        if (lane == 0)
-          bwd::mma_ts_tile(tmem + kColDV, tmem + buf + 32, desc_do_mn + so * kTileD, kIdTS, t > 0);
-        __syncwarp();
-        if (!(ok = mbar_wait_warp(bar(Lay::bDS + (t & 1)), static_cast<uint32_t>(t >> 1) & 1u, wc, 1,
-                                  8)))
-          break;
-        tc_fence_after();
         if (lane == 0) {
-          bwd::mma_ts_tile(tmem + kColDK, tmem + buf, desc_q_mn + sq * kTileD, kIdTS, t > 0);
+          bwd::mma_ts_tile(tmem + kColDV, tmem + buf + 32, desc_do_mn + so * kTileD, kIdTS, t > 0);
           mma_commit(bar(Lay::bACC + (t & 1)));
-          mma_commit(bar(Lay::bQE + sq));
           mma_commit(bar(Lay::bOE + so));
         }
         __syncwarp();
       }
-      // the other issuers' products all completed before the last dS^T was written, so this
-      // commit covers every product of the CTA
-      if (ok && lane == 0) mma_commit(bar(Lay::bEND));
+    }
+    // every S^T and dP^T product completed before the compute warps wrote the last dS^T, so the
+    // commits of the dV and dK issuers after their last products cover every product of the CTA
+    if (ok && warp != 11) {
+      if (lane == 0) mma_commit(bar(Lay::bEND));
       __syncwarp();
     }
     if (!ok) {  // unwinding: wait for every MMA this thread issued
