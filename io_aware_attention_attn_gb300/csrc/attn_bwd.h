@@ -22,6 +22,11 @@
 
 namespace attn {
 
+// Status kind (low byte of the device status word, beside the kinds of the bounded waits): the
+// launch's dynamic shared memory could not hold the dK/dV pass's 1024-byte-aligned layout; the
+// CTA then did nothing.
+constexpr int kStatusSmemLayout = 3;
+
 constexpr int kBwdThreads = 384;    // warp 0 TMA, warps 1, 10, 11 MMA, warps 2..9 column halves
 constexpr int kBwdStages = 2;       // depth of the streamed-tile rings
 constexpr int kBwdStagesQ = 3;      // dK/dV kernel: depth of the Q ring

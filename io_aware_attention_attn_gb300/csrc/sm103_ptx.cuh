@@ -15,9 +15,8 @@ namespace attn {
 // kernel then unwinds (drains its copies and MMAs, frees tensor memory) instead of hanging.
 // --------------------------------------------------------------------------------------------
 // kinds (low byte of the status word): a bounded wait ran out; cu_seqlens was not a valid prefix
-// sum of lengths (the kernel then computed on offsets clamped into [0, N]); the launch's dynamic
-// shared memory could not hold a kernel's 1024-byte-aligned layout (the kernel did nothing)
-enum : int { kStatusTimeout = 1, kStatusBadSeqlens = 2, kStatusSmemLayout = 3 };
+// sum of lengths (the kernel then computed on offsets clamped into [0, N])
+enum : int { kStatusTimeout = 1, kStatusBadSeqlens = 2 };
 // A wait gives up after this many nanoseconds of %globaltimer (one second).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
