@@ -140,9 +140,10 @@ ATTN_API size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int
  * rebuilt tile by tile from the logsumexp the forward saved (CS336 Lecture 5 notes, section 6.2,
  * "反向传播怎么办"), and the gradients follow from the definition by the chain rule:
  * dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with D_i = dO_i . O_i, dQ = scale dS K,
- * dK = scale dS^T Q.  Three kernel launches on `stream`: a row pass (D and lse * log2 e into the
- * workspace), a dK/dV kernel (one CTA per 128-key tile) and a dQ kernel (one CTA per 128-query
- * tile); every output element is written once (deterministic, no atomics).
+ * dK = scale dS^T Q.  Two kernel launches on `stream`: a row pass (D and lse * log2 e into the
+ * workspace), then one grid whose first CTAs run the dK/dV pass (one CTA per 128-key tile) and
+ * the rest the dQ pass (one CTA per 128-query tile); every output element is written once
+ * (deterministic, no atomics).
  * Dense layout only:
  *   q, k, v, o, dout : bf16 [B, H, N, d] (o is the forward's output, dout the gradient of the loss
  *                      with respect to it)         lse : fp32 [B, H, N], the forward's lse output
@@ -162,7 +163,7 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
  * Backward pass of grouped-query / multi-query attention (CS336 Lecture 5 notes, section 6.3):
  * as attn_bwd, except that k, v, dk and dv have H_kv heads ([B, H_kv, N, d]) and query head h
  * reads K/V head h / (H / H_kv).  A K/V head's gradients are the sums over the query heads that
- * share it: the dK/dV kernel runs one CTA per (K/V head, key tile) that visits the query tiles of
+ * share it: the dK/dV pass runs one CTA per (K/V head, key tile) that visits the query tiles of
  * all of them, so the sums accumulate in tensor memory and each element is still written once.
  * H_kv must divide H, else ATTN_ERR_SHAPE.  The workspace is attn_bwd_workspace_bytes(B,H,N,d).
  */
@@ -175,7 +176,7 @@ ATTN_API int attn_bwd_gqa(const void* q, const void* k, const void* v, const voi
  * Backward pass on a packed batch of variable-length sequences (the layout of attn_fwd with
  * cu_seqlens): q, o, dout, dq [H, T, d]; k, v, dk, dv [H_kv, T, d]; lse [H, T]; cu_seqlens
  * int32[B + 1] on the device, B = number of sequences, T = total rows.  Sequences are independent;
- * grouped-query heads as attn_bwd_gqa (H_kv = H for multi-head).  The kernels run one CTA per
+ * grouped-query heads as attn_bwd_gqa (H_kv = H for multi-head).  The tile passes run one CTA per
  * (head, 128-row tile of a sequence), found by a scan of cu_seqlens; offsets are clamped into
  * [0, T].  workspace: attn_bwd_varlen_workspace_bytes(B, H, T, d) bytes, 256-byte aligned.
  * cu_seqlens NULL: ATTN_ERR_NULL.  Returns an attn_status.
