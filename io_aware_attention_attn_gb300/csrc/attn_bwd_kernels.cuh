@@ -1,30 +1,34 @@
-// attn_bwd_kernels.cuh -- tcgen05 kernels of the attention backward pass for sm_103a (GB300).
+// attn_bwd_kernels.cuh -- tcgen05 kernel of the attention backward pass for sm_103a (GB300).
 //
-// Both tile kernels keep one 128-row tile resident, stream the other operand's tiles through
-// TMA-fed shared-memory rings, and rebuild P from the saved logsumexp instead of reading any
-// N x N matrix (CS336 Lecture 5 notes, section 6.2, "反向传播怎么办").
+// One launch runs two tile passes: CTAs 0 .. n_kv-1 the dK/dV pass, the others the dQ pass.  Each
+// CTA keeps one 128-row tile resident, streams the other operand's tiles through TMA-fed
+// shared-memory rings, and rebuilds P from the saved logsumexp instead of reading any N x N
+// matrix (CS336 Lecture 5 notes, section 6.2, "反向传播怎么办").
 //
 // Warp roles (384 threads): warp 0 TMA producer; warp 1 TMEM owner and an MMA issuer (lane 0);
-// warps 10 and 11 MMA issuers; warps 2..9 compute.  Each kernel's products form three streams
-// that only meet through barriers (dK/dV: S^T, dP^T, and dV with dK; dQ: S, dP, dQ), one per
-// issuing thread: an MMA issue blocks until the tensor pipe accepts it, so a thread issuing two
-// streams held the second one back behind every issue and every wait of the first.  A compute thread owns one row of the resident tile (its TMEM lane: warp
-// w may access lanes 32*(w%4)..+31) and one half of the streamed tile's 128 columns: warps 2..5
-// take columns 0..63, warps 6..9 columns 64..127.
+// warps 10 and 11 MMA issuers; warps 2..9 compute.  Each pass's products form three streams that
+// meet only through barriers (dK/dV: S^T with dK, dP^T, dV; dQ: S, dP, dQ), one per issuing
+// thread: an MMA issue blocks until the tensor pipe accepts it, so a thread issuing two streams
+// held the second one back behind every issue and every wait of the first.  A compute thread owns
+// one row of the resident tile (its TMEM lane: warp w may access lanes 32*(w%4)..+31) and one
+// half of the streamed tile's 128 columns: warps 2..5 take columns 0..63, warps 6..9 64..127.
 //
-// dK/dV kernel (rows = 128 keys of tile j, columns = 128 queries of tile i), per query tile:
-//   S^T  = K_j Q_i^T      (SS MMA into TMEM columns 0..127)
-//   dP^T = V_j dO_i^T     (SS MMA into TMEM columns 128..255)
-//   P^T  = 2^(S^T scale log2e - lse2_i) per element, bf16, written back over the first 32
-//          columns of each half of S^T; dS^T = P^T * (dP^T - D_i), bf16, over dP^T likewise
+// dK/dV pass (rows = 128 keys of tile j, columns = 128 queries of tile i), query tile t in one of
+// two 128-column TMEM buffers (t mod 2):
+//   S^T  = K_j Q_i^T      (SS MMA into the buffer)
+//   P^T  = 2^(S^T scale log2e - lse2_i) per element, kept in fp32 registers
+//   dP^T = V_j dO_i^T     (SS MMA over the same buffer, once every compute thread has loaded S^T)
+//   P^T as bf16 over the buffer's last 32 columns of each half, then dS^T = P^T * (dP^T - D_i) as
+//          bf16 over the first 32 (signalled separately: dV starts while dS is formed)
 //   dV  += P^T dO_i       (TS MMA, A = P^T from TMEM, B = dO_i MN-major; TMEM 256..256+D)
 //   dK  += dS^T Q_i       (TS MMA, A = dS^T from TMEM, B = Q_i MN-major; TMEM 256+D..)
-// dQ kernel (rows = 128 queries of tile i, columns = 128 keys of tile j), per key tile:
-//   S = Q_i K_j^T, dP = dO_i V_j^T (SS), P and dS as above with per-row lse2 and D,
+//   the buffer takes S^T of tile t+2 once dV and dK of tile t have completed
+// dQ pass (rows = 128 queries of tile i, columns = 128 keys of tile j), per key tile:
+//   S = Q_i K_j^T (TMEM 0..127, rewritten once every compute thread has loaded it),
+//   dP = dO_i V_j^T (two buffers at 128 and 384), P and dS as above with per-row lse2 and D,
 //   dQ += dS K_j          (TS MMA, B = K_j MN-major; TMEM 256..256+D)
-// Each TS MMA reads its A operand from the columns it was written to, so the next tile's SS MMA
-// into the same columns waits for that TS MMA to complete (tcgen05 MMAs with different
-// accumulators are not ordered).
+// An SS product into columns that a TS product reads its A operand from waits for that TS
+// product to complete (tcgen05 MMAs with different accumulators are not ordered).
 #pragma once
 
 #include <cuda.h>
