@@ -22,6 +22,13 @@
 
 namespace attn {
 
+// Programmatic dependent launch: the tile kernel is launched as the row pass's blocks finish, sets
+// up its barriers and tensor memory, and waits here for the row pass's grid to complete (and its
+// writes to be visible) before it reads the planes.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Status kind (low byte of the device status word, beside the kinds of the bounded waits): the
 // launch's dynamic shared memory could not hold the dK/dV pass's 1024-byte-aligned layout; the
 // CTA then did nothing.

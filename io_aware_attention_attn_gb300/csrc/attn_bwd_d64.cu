@@ -35,7 +35,19 @@ cudaError_t launch(const BwdParams& p, cudaStream_t stream) {
   const long long units = VARLEN ? p.n_tiles : static_cast<long long>(p.n_tiles) * p.B;
   const long long n_kv = units * p.H_kv, n_q = units * p.H;
   if (n_kv + n_q > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  kernel<<<static_cast<int>(n_kv + n_q), kBwdThreads, kSmem, stream>>>(p, static_cast<int>(n_kv));
+  // programmatic dependent launch: the CTAs set up while the row pass finishes, then wait for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_kv + n_q));
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, p, static_cast<int>(n_kv));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

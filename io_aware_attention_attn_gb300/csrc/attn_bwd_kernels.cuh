@@ -190,6 +190,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dependency_wait();  // the row pass's -lse2 / -D planes are complete from here on
   const uint32_t tmem = misc[0];
   // two 128-column buffers: query tile t uses buffer t & 1 for S^T_t, then (once the compute warps
   // have loaded S^T_t) for dP^T_t, then for the bf16 P^T_t and dS^T_t the dV and dK products read
@@ -560,6 +561,7 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, const int L, uint
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dependency_wait();  // the row pass's -lse2 / -D planes are complete from here on
   const uint32_t tmem = misc[0];
   // S at 0, dQ at 256, dP / dS double-buffered at 128 and 384 (key tile jj uses buffer jj & 1)
   constexpr uint32_t kColS = 0, kColDQ = 256;
