@@ -271,6 +271,11 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o,
       encode_rows_map(&p.tm_v, v, d, N, kv_heads) != CUDA_SUCCESS ||
       encode_rows_map(&p.tm_do, dout, d, N, heads) != CUDA_SUCCESS)
     return ATTN_ERR_LAUNCH;
+  // head dim 128: the tile passes write dQ, dK, dV by TMA stores of 32-row staging tiles
+  if (d == 128 && (encode_rows_map(&p.tm_dq, dq, d, N, heads, 32u) != CUDA_SUCCESS ||
+                   encode_rows_map(&p.tm_dk, dk, d, N, kv_heads, 32u) != CUDA_SUCCESS ||
+                   encode_rows_map(&p.tm_dv, dv, d, N, kv_heads, 32u) != CUDA_SUCCESS))
+    return ATTN_ERR_LAUNCH;
   p.H_kv = Hkv;
   p.group = H / Hkv;
   p.dq = static_cast<__nv_bfloat16*>(dq);

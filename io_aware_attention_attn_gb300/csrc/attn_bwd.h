@@ -43,6 +43,9 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
+  CUtensorMap tm_dq;  // dense head dim 128: outputs, box {64, 32, 1}, 128-byte swizzle (TMA stores)
+  CUtensorMap tm_dk;
+  CUtensorMap tm_dv;
   __nv_bfloat16* dq;  // outputs [B, H, N, D] bf16
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;

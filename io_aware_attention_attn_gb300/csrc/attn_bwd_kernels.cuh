@@ -92,6 +92,28 @@ __device__ __forceinline__ void store_row_half(uint32_t col, float mul, __nv_bfl
   }
 }
 
+// One row's 64-column half of a 128-wide fp32 accumulator (TMEM columns col .. col + 63), times
+// `mul`, as bf16 into row `lane` of a warp's 32-row staging tile: 128-byte rows, 16-byte chunks
+// XOR-swizzled by row (the output tensor map's 128-byte swizzle, and no bank conflicts).
+__device__ __forceinline__ void stage_row_half128(uint32_t col, float mul, uint32_t stage,
+                                                  int lane) {
+  #pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t v[32];
+    tmem_ld32(col + 32 * c, v);
+    tmem_wait_ld_regs(v);
+    #pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = 4 * c + q;
+      st_shared_v4(stage + lane * 128 + ((chunk ^ (lane & 7)) << 4),
+                   pack_bf16x2(u2f(v[8 * q + 0]) * mul, u2f(v[8 * q + 1]) * mul),
+                   pack_bf16x2(u2f(v[8 * q + 2]) * mul, u2f(v[8 * q + 3]) * mul),
+                   pack_bf16x2(u2f(v[8 * q + 4]) * mul, u2f(v[8 * q + 5]) * mul),
+                   pack_bf16x2(u2f(v[8 * q + 6]) * mul, u2f(v[8 * q + 7]) * mul));
+    }
+  }
+}
+
 }  // namespace bwd
 
 // =============================================================================== dK / dV kernel
@@ -465,13 +487,32 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
     if (ok) ok = mbar_wait_warp(bar(Lay::bEND), 0, wc, 2, 13);
     if (ok) {
       tc_fence_after();
-      const int key = j * kBN + r;
-      const bool valid = key < seq_len;
-      const size_t row = static_cast<size_t>(z) * p.N + y0 + (valid ? key : 0);
-      bwd::store_row_half<D>(t_lane + kColDV + half * (D / 2), 1.f, p.dv + row * D + half * (D / 2),
-                             valid);
-      bwd::store_row_half<D>(t_lane + kColDK + half * (D / 2), p.scale,
-                             p.dk + row * D + half * (D / 2), valid);
+      if constexpr (D == 128 && !VARLEN) {
+        // dV and scale dK through 32-row staging tiles in the idle Q ring (every product has
+        // completed, so no load is in flight), written by TMA stores that clip rows past N;
+        // stores from the threads wrote 16 bytes to each of 32 rows per instruction
+        const uint32_t stage = sbase + Lay::kQ + static_cast<uint32_t>(warp - 2) * 8192u;
+        bwd::stage_row_half128(t_lane + kColDV + half * 64, 1.f, stage, lane);
+        bwd::stage_row_half128(t_lane + kColDK + half * 64, p.scale, stage + 4096u, lane);
+        fence_proxy_async_smem();  // the generic-proxy writes, before the async-proxy reads
+        __syncwarp();
+        const int row0 = j * kBN + quarter * 32;
+        if (lane == 0 && row0 < seq_len) {
+          tma_store_3d(&p.tm_dv, stage, 64 * half, row0, z);
+          tma_store_3d(&p.tm_dk, stage + 4096u, 64 * half, row0, z);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the staging area stays valid until the stores have read it
+        }
+        __syncwarp();
+      } else {
+        const int key = j * kBN + r;
+        const bool valid = key < seq_len;
+        const size_t row = static_cast<size_t>(z) * p.N + y0 + (valid ? key : 0);
+        bwd::store_row_half<D>(t_lane + kColDV + half * (D / 2), 1.f,
+                               p.dv + row * D + half * (D / 2), valid);
+        bwd::store_row_half<D>(t_lane + kColDK + half * (D / 2), p.scale,
+                               p.dk + row * D + half * (D / 2), valid);
+      }
     }
   }
   tc_fence_before();
@@ -769,10 +810,25 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, const int L, uint
                           static_cast<uint32_t>((n_kv - 1) >> 1) & 1u, wc, 2, 10);
     if (ok) {
       tc_fence_after();
-      const bool valid = row < seq_len;
-      const size_t grow = static_cast<size_t>(z) * p.N + y0 + (valid ? row : 0);
-      bwd::store_row_half<D>(t_lane + kColDQ + half * (D / 2), p.scale,
-                             p.dq + grow * D + half * (D / 2), valid);
+      if constexpr (D == 128 && !VARLEN) {
+        // scale dQ through a 32-row staging tile in the idle K ring, written by a TMA store
+        const uint32_t stage = sbase + Lay::kK + static_cast<uint32_t>(warp - 2) * 4096u;
+        bwd::stage_row_half128(t_lane + kColDQ + half * 64, p.scale, stage, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int row0 = i * kBM + quarter * 32;
+        if (lane == 0 && row0 < seq_len) {
+          tma_store_3d(&p.tm_dq, stage, 64 * half, row0, z);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        __syncwarp();
+      } else {
+        const bool valid = row < seq_len;
+        const size_t grow = static_cast<size_t>(z) * p.N + y0 + (valid ? row : 0);
+        bwd::store_row_half<D>(t_lane + kColDQ + half * (D / 2), p.scale,
+                               p.dq + grow * D + half * (D / 2), valid);
+      }
     }
   }
   tc_fence_before();
