@@ -340,6 +340,11 @@ extern "C" int attn_bwd_varlen(const void* q, const void* k, const void* v, cons
       encode_rows_map(&p.tm_v, v, d, T, H_kv) != CUDA_SUCCESS ||
       encode_rows_map(&p.tm_do, dout, d, T, H) != CUDA_SUCCESS)
     return ATTN_ERR_LAUNCH;
+  // head dim 128: warps whose 32 rows lie inside their sequence write by TMA stores
+  if (d == 128 && (encode_rows_map(&p.tm_dq, dq, d, T, H, 32u) != CUDA_SUCCESS ||
+                   encode_rows_map(&p.tm_dk, dk, d, T, H_kv, 32u) != CUDA_SUCCESS ||
+                   encode_rows_map(&p.tm_dv, dv, d, T, H_kv, 32u) != CUDA_SUCCESS))
+    return ATTN_ERR_LAUNCH;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);

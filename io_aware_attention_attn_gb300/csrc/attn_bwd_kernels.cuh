@@ -487,19 +487,23 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
     if (ok) ok = mbar_wait_warp(bar(Lay::bEND), 0, wc, 2, 13);
     if (ok) {
       tc_fence_after();
-      if constexpr (D == 128 && !VARLEN) {
-        // dV and scale dK through 32-row staging tiles in the idle Q ring (every product has
-        // completed, so no load is in flight), written by TMA stores that clip rows past N;
-        // stores from the threads wrote 16 bytes to each of 32 rows per instruction
+      // head dim 128: dV and scale dK through 32-row staging tiles in the idle Q ring (every
+      // product has completed, so no load is in flight), written by TMA stores; on dense batches
+      // the tensor maps clip rows past N, on packed batches only warps whose 32 rows all belong
+      // to the sequence take this path (rows past its end are the next sequence's).  Stores from
+      // the threads wrote 16 bytes to each of 32 rows per instruction.
+      const int row0 = j * kBN + quarter * 32;  // this warp's first key row in the sequence
+      bool staged = false;
+      if constexpr (D == 128) staged = !VARLEN || row0 + 32 <= seq_len;
+      if (staged) {
         const uint32_t stage = sbase + Lay::kQ + static_cast<uint32_t>(warp - 2) * 8192u;
         bwd::stage_row_half128(t_lane + kColDV + half * 64, 1.f, stage, lane);
         bwd::stage_row_half128(t_lane + kColDK + half * 64, p.scale, stage + 4096u, lane);
         fence_proxy_async_smem();  // the generic-proxy writes, before the async-proxy reads
         __syncwarp();
-        const int row0 = j * kBN + quarter * 32;
         if (lane == 0 && row0 < seq_len) {
-          tma_store_3d(&p.tm_dv, stage, 64 * half, row0, z);
-          tma_store_3d(&p.tm_dk, stage + 4096u, 64 * half, row0, z);
+          tma_store_3d(&p.tm_dv, stage, 64 * half, y0 + row0, z);
+          tma_store_3d(&p.tm_dk, stage + 4096u, 64 * half, y0 + row0, z);
           bulk_commit_group();
           bulk_wait_group_read0();  // the staging area stays valid until the stores have read it
         }
@@ -810,15 +814,18 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, const int L, uint
                           static_cast<uint32_t>((n_kv - 1) >> 1) & 1u, wc, 2, 10);
     if (ok) {
       tc_fence_after();
-      if constexpr (D == 128 && !VARLEN) {
-        // scale dQ through a 32-row staging tile in the idle K ring, written by a TMA store
+      const int row0 = i * kBM + quarter * 32;  // this warp's first query row in the sequence
+      bool staged = false;
+      if constexpr (D == 128) staged = !VARLEN || row0 + 32 <= seq_len;
+      if (staged) {
+        // scale dQ through a 32-row staging tile in the idle K ring, written by a TMA store (the
+        // conditions of the dK/dV pass's epilogue)
         const uint32_t stage = sbase + Lay::kK + static_cast<uint32_t>(warp - 2) * 4096u;
         bwd::stage_row_half128(t_lane + kColDQ + half * 64, p.scale, stage, lane);
         fence_proxy_async_smem();
         __syncwarp();
-        const int row0 = i * kBM + quarter * 32;
         if (lane == 0 && row0 < seq_len) {
-          tma_store_3d(&p.tm_dq, stage, 64 * half, row0, z);
+          tma_store_3d(&p.tm_dq, stage, 64 * half, y0 + row0, z);
           bulk_commit_group();
           bulk_wait_group_read0();
         }
