@@ -67,7 +67,7 @@ struct BwdParams {
 // (S^T of query tile t+2 is issued while tile t+1 is being processed, so its Q tile must have
 // landed a tile earlier), dO_i with its -D slice through a kBwdStages ring.  At head dim 128 the
 // tiles take 224 KB; the layout then fits the 227 KB limit only if the dynamic shared memory
-// starts within 280 bytes of a 1024-byte boundary (the kernel checks, and reports
+// starts within 272 bytes of a 1024-byte boundary (the kernel checks, and reports
 // kStatusSmemLayout instead of running otherwise).
 template <int D>
 struct BwdKvLayout {
@@ -92,6 +92,7 @@ struct BwdKvLayout {
     bDS = bP + 2,              // dS^T (bf16) written over dP^T (256 arrivals) [2 buffers]
     bACC = bDS + 2,            // dV += P^T dO and dK += dS^T Q completed  [2 buffers]
     bEND = bACC + 2,           // every product of the CTA completed (dV and dK issuers)
+    bVEND,                     // the last dV product completed
     bDR,                       // drain after an abort, one per issuer [3]
     kNumBars = bDR + 3
   };

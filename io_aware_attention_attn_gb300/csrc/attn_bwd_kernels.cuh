@@ -156,6 +156,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
     mbar_init(bar(Lay::bACC), 2);      // a commit of each of the dV and dK issuers
     mbar_init(bar(Lay::bACC + 1), 2);
     mbar_init(bar(Lay::bEND), 2);
+    mbar_init(bar(Lay::bVEND), 1);
     for (int d = 0; d < 3; ++d) mbar_init(bar(Lay::bDR + d), 1);
     fence_barrier_init();
     misc[1] = 0;
@@ -361,6 +362,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
           bwd::mma_ts_tile(tmem + kColDV, tmem + buf + 32, desc_do_mn + so * kTileD, kIdTS, t > 0);
           mma_commit(bar(Lay::bACC + (t & 1)));
           mma_commit(bar(Lay::bOE + so));
+          if (t == n_it - 1) mma_commit(bar(Lay::bVEND));  // dV final: its epilogue may start
         }
         __syncwarp();
       }
@@ -483,29 +485,41 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, const int L, ui
       tc_fence_before();
       mbar_arrive(bar(Lay::bDS + (t & 1)));
     }
-    // epilogue, once every product of the CTA has completed
+    // epilogue: dV once its last product has completed (the last dK product may still run),
+    // then scale dK once every product of the CTA has completed.  Head dim 128: 32-row staging
+    // tiles in the dO ring (idle once the last dV product, the last reader of dO, has completed;
+    // every load has landed), written by TMA stores; on dense batches the tensor maps clip rows
+    // past N, on packed batches only warps whose 32 rows all belong to the sequence take this
+    // path (rows past its end are the next sequence's).  Stores from the threads wrote 16 bytes
+    // to each of 32 rows per instruction.
+    if (ok) ok = mbar_wait_warp(bar(Lay::bVEND), 0, wc, 2, 14);
+    const int row0 = j * kBN + quarter * 32;  // this warp's first key row in the sequence
+    bool staged = false;
+    if constexpr (D == 128) staged = !VARLEN || row0 + 32 <= seq_len;
+    const uint32_t stage_v = sbase + Lay::kDO + static_cast<uint32_t>(warp - 2) * 4096u;
+    const uint32_t stage_k = stage_v + static_cast<uint32_t>(Lay::kTile);  // the second dO stage
+    if (ok && staged) {
+      tc_fence_after();
+      bwd::stage_row_half128(t_lane + kColDV + half * 64, 1.f, stage_v, lane);
+      fence_proxy_async_smem();  // the generic-proxy writes, before the async-proxy reads
+      __syncwarp();
+      if (lane == 0 && row0 < seq_len) {
+        tma_store_3d(&p.tm_dv, stage_v, 64 * half, y0 + row0, z);
+        bulk_commit_group();
+      }
+      __syncwarp();
+    }
     if (ok) ok = mbar_wait_warp(bar(Lay::bEND), 0, wc, 2, 13);
     if (ok) {
       tc_fence_after();
-      // head dim 128: dV and scale dK through 32-row staging tiles in the idle Q ring (every
-      // product has completed, so no load is in flight), written by TMA stores; on dense batches
-      // the tensor maps clip rows past N, on packed batches only warps whose 32 rows all belong
-      // to the sequence take this path (rows past its end are the next sequence's).  Stores from
-      // the threads wrote 16 bytes to each of 32 rows per instruction.
-      const int row0 = j * kBN + quarter * 32;  // this warp's first key row in the sequence
-      bool staged = false;
-      if constexpr (D == 128) staged = !VARLEN || row0 + 32 <= seq_len;
       if (staged) {
-        const uint32_t stage = sbase + Lay::kQ + static_cast<uint32_t>(warp - 2) * 8192u;
-        bwd::stage_row_half128(t_lane + kColDV + half * 64, 1.f, stage, lane);
-        bwd::stage_row_half128(t_lane + kColDK + half * 64, p.scale, stage + 4096u, lane);
-        fence_proxy_async_smem();  // the generic-proxy writes, before the async-proxy reads
+        bwd::stage_row_half128(t_lane + kColDK + half * 64, p.scale, stage_k, lane);
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && row0 < seq_len) {
-          tma_store_3d(&p.tm_dv, stage, 64 * half, y0 + row0, z);
-          tma_store_3d(&p.tm_dk, stage + 4096u, 64 * half, y0 + row0, z);
+          tma_store_3d(&p.tm_dk, stage_k, 64 * half, y0 + row0, z);
           bulk_commit_group();
-          bulk_wait_group_read0();  // the staging area stays valid until the stores have read it
+          bulk_wait_group_read0();  // the staging areas stay valid until the stores have read them
         }
         __syncwarp();
       } else {
