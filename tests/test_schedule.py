@@ -7,6 +7,11 @@ them and check what the kernel relies on: every unit is taken by exactly one clu
 cluster's units come in increasing rounds, the slices of a pair cover its key tiles exactly once,
 and a causal pair's key range reaches the diagonal of its last row.  The slice-count choice made
 by the library is checked through the C ABI (no GPU needed).
+
+The backward's tile passes are restated the same way: the warp scan that maps a packed batch's
+tile slot to (sequence, tile) must reach every tile of every sequence exactly once within the
+slots the host sizes the workspace for, with the slot equal to its row block in the -lse2 / -D
+planes; the dense slot orders must cover every (head, tile) once, heaviest first when causal.
 """
 import pytest
 
@@ -195,3 +200,94 @@ def test_dense_causal_order_takes_every_pair_once_heaviest_band_first(n_qt, BH):
     assert sorted(units) == sorted((z, pt) for z in range(BH) for pt in range(n_qt))
     levels = [pt // (DENSE_BAND if n_qt > 2 * DENSE_BAND else 1) for _, pt in units]
     assert levels == sorted(levels, reverse=True)
+
+
+# ---- backward: tile slots of packed batches, and the dense slot orders of the two tile passes
+
+def bwd_locate_tile(cu, n_seqs, N, slot):
+    """The backward kernels' warp scan over cu_seqlens, 32 sequences per step, offsets clamped
+    into [0, N]: (start row, length, tile within the sequence, tiles of the earlier sequences);
+    tile -1 for a slot past the last tile."""
+    import itertools
+    remaining, before = slot, 0
+    for b0 in range(0, n_seqs, 32):
+        spans, nts = [], []
+        for lane in range(32):
+            s = b0 + lane
+            a = e = 0
+            if s < n_seqs:
+                a = min(max(cu[s], 0), N)
+                e = min(max(cu[s + 1], a), N)
+            spans.append((a, e))
+            nts.append((e - a + BM - 1) // BM)
+        incl = list(itertools.accumulate(nts))
+        if remaining < incl[-1]:
+            src = next(lane for lane in range(32) if incl[lane] - nts[lane] <= remaining < incl[lane])
+            a, e = spans[src]
+            ex = incl[src] - nts[src]
+            return a, e - a, remaining - ex, before + ex
+        remaining -= incl[-1]
+        before += incl[-1]
+    return 0, 0, -1, 0
+
+
+@pytest.mark.parametrize("cu,N", [
+    ([0, 1, 1, 701, 2201, 2457, 2714, 5714, 5714, 5843, 6867, 7378, 9427], 9427),
+    ([0] + [128 * (k + 1) for k in range(45)], 45 * 128),   # more than 32 sequences
+    ([0, 300], 300),
+    ([0, 0, 0, 5], 5),
+    ([0, 257, 200, 900, 5000], 900),   # decreasing and past-the-end offsets are clamped
+])
+def test_bwd_packed_slots_cover_every_tile_once(cu, N):
+    n_seqs = len(cu) - 1
+    n_slots = (N + BM - 1) // BM + n_seqs   # the host's slots per head (workspace planes)
+    expected = set()
+    for s in range(n_seqs):
+        a = min(max(cu[s], 0), N)
+        e = min(max(cu[s + 1], a), N)
+        expected |= {(a, t) for t in range((e - a + BM - 1) // BM)}
+    assert len(expected) <= n_slots
+    seen = set()
+    for slot in range(n_slots + 3):
+        a, length, tile, base = bwd_locate_tile(cu, n_seqs, N, slot)
+        if tile < 0:
+            assert slot >= len(expected)
+            continue
+        assert (a, tile) not in seen
+        seen.add((a, tile))
+        assert base + tile == slot        # the -lse2 / -D plane rows of the slot: 128 * slot ..
+        assert 0 <= tile * BM < length and a + length <= N
+    assert seen == expected
+
+
+def bwd_dkdv_slot(L, B, H_kv, n_tiles, causal):
+    if causal:
+        return L % (B * H_kv), L // (B * H_kv)
+    return L // n_tiles, L % n_tiles
+
+
+def bwd_dq_slot(L, B, H, n_tiles, causal):
+    if causal:
+        return L % (B * H), n_tiles - 1 - L // (B * H)
+    return L // n_tiles, L % n_tiles
+
+
+@pytest.mark.parametrize("B,H,H_kv,n_tiles", [(1, 1, 1, 1), (2, 32, 32, 32), (2, 32, 8, 32),
+                                               (3, 6, 2, 5), (4, 16, 16, 8)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_dense_slots_cover_every_tile_once(B, H, H_kv, n_tiles, causal):
+    kv = [bwd_dkdv_slot(L, B, H_kv, n_tiles, causal) for L in range(B * H_kv * n_tiles)]
+    assert sorted(kv) == [(z, j) for z in range(B * H_kv) for j in range(n_tiles)]
+    dq = [bwd_dq_slot(L, B, H, n_tiles, causal) for L in range(B * H * n_tiles)]
+    assert sorted(dq) == [(z, i) for z in range(B * H) for i in range(n_tiles)]
+    if causal:
+        # heaviest CTAs first: a key tile j visits n_tiles - j query tiles, a query tile i visits
+        # i + 1 key tiles
+        kv_work = [n_tiles - j for _, j in kv]
+        dq_work = [i + 1 for _, i in dq]
+        assert kv_work == sorted(kv_work, reverse=True)
+        assert dq_work == sorted(dq_work, reverse=True)
+    else:
+        # a head's tiles are adjacent, so its streamed tiles are shared in L2
+        assert [z for z, _ in kv] == sorted(z for z, _ in kv)
+        assert [z for z, _ in dq] == sorted(z for z, _ in dq)
