@@ -309,6 +309,17 @@ ATTN_API int attn_selftest_mma(const void* a, const void* b, float* d, int mode,
  */
 ATTN_API int attn_selftest_wait_timeout(void* stream);
 
+/*
+ * Diagnostic of attn_quantize_fp8's division: for every positive finite bf16 number amax and every
+ * bf16 x with |x| <= amax (both signs, about 1.07e9 pairs), compares the E4M3 code the quantizer
+ * forms for x at the tile scale amax / 448 with the code of the correctly rounded fp32 quotient
+ * (the per-tile scaling of CS336 Lecture 5 notes, section 3.1), and writes the number of pairs
+ * that differ to *mismatches.  mismatches: device pointer to one 8-byte-aligned 64-bit counter,
+ * which the call zeroes first.  Asynchronous on `stream` (about a second of GPU time); returns an
+ * attn_status (the launch only).
+ */
+ATTN_API int attn_selftest_fp8_quotients(unsigned long long* mismatches, void* stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 ATTN_API int attn_version(void);
 

@@ -45,6 +45,7 @@ SIGNATURES = {
     "attn_get_last_device_error": (_I, [_P]),
     "attn_selftest_mma": (_I, [_P, _P, _P, _I, _I, _P]),
     "attn_selftest_wait_timeout": (_I, [_P]),
+    "attn_selftest_fp8_quotients": (_I, [_P, _P]),
     "attn_version": (_I, []),
 }
 
@@ -356,6 +357,18 @@ def selftest_wait_timeout(stream=None):
     dev = torch.device("cuda", torch.cuda.current_device())
     _check("attn_selftest_wait_timeout",
            lib().attn_selftest_wait_timeout(_stream_handle(stream, dev)))
+
+
+def selftest_fp8_quotients(stream=None) -> int:
+    """Pairs (x, tile maximum) whose quantizer code differs from the code of the IEEE quotient
+    (see attn_selftest_fp8_quotients in the header); synchronises the stream."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = torch.zeros(1, dtype=torch.int64, device=dev)
+    _check("attn_selftest_fp8_quotients",
+           lib().attn_selftest_fp8_quotients(out.data_ptr(), _stream_handle(stream, dev)))
+    torch.cuda.synchronize(dev)
+    return int(out.item())
 
 
 def decode_status(code: int) -> dict:

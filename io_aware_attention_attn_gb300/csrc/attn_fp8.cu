@@ -3,7 +3,7 @@
 // Quantization of a bf16 tensor [B*H][N][d], per tile of 128 rows of a head (CS336 Lecture 5
 // notes, section 3.1: E4M3 for forward activations, with per-tile scaling):
 //   scale = amax / 448 in fp32 (1 for an all-zero tile), code = E4M3 round-to-nearest-even of
-//   x / scale (fp32 IEEE division), saturating at +-448.
+//   x / scale rounded to nearest fp32 (the IEEE quotient), saturating at +-448.
 // Codes are written row-major [B*H][N][d], or transposed [B*H][d][Npad] (Npad = N rounded up to
 // 128, padding codes 0) for the V operand of the FP8 forward.
 #include <atomic>
@@ -17,13 +17,36 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 
+// x / sc rounded to nearest fp32, from rc = RN(1 / sc) and one remainder correction: with
+// q0 = RN(x rc), the remainder x - sc q0 is exact under a fused multiply-add and RN(q0 + rem rc)
+// is the rounded quotient (the correction step of FMA-based division: P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1),
+// 1990).  The sign comes from x, so -0 stays -0.  Used for the scales of tiles whose reciprocal
+// is far from the fp32 range's ends; attn_selftest_fp8_quotients compares the codes it gives
+// with those of the IEEE division for every bf16 value and every scale a bf16 tile can have.
+constexpr float kFastQuotientMinScale = 0x1p-100f;
+
+__device__ __forceinline__ float quotient_rn(float x, float sc, float rc) {
+  const float q0 = __fmul_rn(x, rc);
+  return copysignf(__fmaf_rn(__fmaf_rn(-sc, q0, x), rc, q0), x);
+}
+
+// E4M3 codes of x0 / sc and x1 / sc (x0 in the low byte), as the quantizer forms them.
+__device__ __forceinline__ uint16_t code_pair(float x0, float x1, float sc, float rc, bool fast) {
+  return fast ? pack_e4m3x2(quotient_rn(x0, sc, rc), quotient_rn(x1, sc, rc))
+              : pack_e4m3x2(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
+}
+
+// One block per (head slice z, 128-row tile t); thread 2r + h holds half h of row r.  The tile
+// stays in registers as packed bf16 (D/4 words a thread), every load issued before the first use,
+// so four blocks fit on an SM with their whole tiles (32 KB each at d = 128) in flight.
 template <int D>
-__global__ void __launch_bounds__(kQuantThreads) quantize_fp8_kernel(
+__global__ void __launch_bounds__(kQuantThreads, 4) quantize_fp8_kernel(
     const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes, float* __restrict__ scales,
     int N, int n_tiles, int n_pad, int transpose) {
   constexpr int kPer = D / 2;  // elements per thread: row = tid / 2, half = tid % 2
   __shared__ float red[kQuantThreads / 32];
-  __shared__ float s_scale;
+  __shared__ float s_scale, s_rcp;
   __shared__ __align__(16) uint8_t tile_t[D][kBM + 16];  // transposed codes (transpose only)
   const int z = blockIdx.x / n_tiles;
   const int t = blockIdx.x % n_tiles;
@@ -31,42 +54,46 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_fp8_kernel(
   const int c0 = (threadIdx.x & 1) * kPer;
   const int row = t * kBM + r;
   const bool valid = row < N;
-  float v[kPer];
+  uint4 w[kPer / 8];  // 8 bf16 values each
   const __nv_bfloat16* src = x + (static_cast<size_t>(z) * N + (valid ? row : 0)) * D + c0;
   #pragma unroll
-  for (int i = 0; i < kPer / 8; ++i) {
-    uint4 w = valid ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-    #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 f = __bfloat1622float2(h[q]);
-      v[8 * i + 2 * q] = f.x;
-      v[8 * i + 2 * q + 1] = f.y;
-    }
-  }
-  float amax = 0.f;
+  for (int i = 0; i < kPer / 8; ++i)
+    w[i] = valid ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
+  // |x| maximum in bf16 (the maximum of bf16 values is one of them: exact)
+  __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
   #pragma unroll
-  for (int i = 0; i < kPer; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  for (int i = 0; i < kPer / 8; ++i) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    #pragma unroll
+    for (int q = 0; q < 4; ++q) m2 = __hmax2(m2, __habs2(h[q]));
+  }
+  float amax = fmaxf(__low2float(m2), __high2float(m2));
   #pragma unroll
   for (int s = 16; s > 0; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
   if (threadIdx.x == 0) {
     float m = 0.f;
-    for (int w = 0; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
+    for (int i = 0; i < kQuantThreads / 32; ++i) m = fmaxf(m, red[i]);
     const float sc = m > 0.f ? __fdiv_rn(m, 448.f) : 1.f;
     s_scale = sc;
+    s_rcp = __frcp_rn(sc);
     scales[blockIdx.x] = sc;
   }
   __syncthreads();
-  const float sc = s_scale;
+  const float sc = s_scale, rc = s_rcp;
+  const bool fast = sc >= kFastQuotientMinScale;
   uint32_t w32[kPer / 4];
   #pragma unroll
-  for (int i = 0; i < kPer / 4; ++i)
-    w32[i] = static_cast<uint32_t>(pack_e4m3x2(__fdiv_rn(v[4 * i], sc), __fdiv_rn(v[4 * i + 1], sc))) |
-             (static_cast<uint32_t>(pack_e4m3x2(__fdiv_rn(v[4 * i + 2], sc),
-                                                __fdiv_rn(v[4 * i + 3], sc)))
-              << 16);
+  for (int i = 0; i < kPer / 8; ++i) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    #pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float2 a = __bfloat1622float2(h[2 * q]), b = __bfloat1622float2(h[2 * q + 1]);
+      w32[2 * i + q] = static_cast<uint32_t>(code_pair(a.x, a.y, sc, rc, fast)) |
+                       (static_cast<uint32_t>(code_pair(b.x, b.y, sc, rc, fast)) << 16);
+    }
+  }
   if (!transpose) {
     if (valid) {
       uint4* dst = reinterpret_cast<uint4*>(codes + (static_cast<size_t>(z) * N + row) * D + c0);
@@ -103,6 +130,37 @@ cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scales, int B
   else
     quantize_fp8_kernel<128><<<static_cast<int>(blocks), kQuantThreads, 0, stream>>>(
         xb, cb, scales, N, n_tiles, n_tiles * kBM, transpose ? 1 : 0);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// Block b takes amax = the positive finite bf16 number with bits b + 1 (0x0001 .. 0x7F7F) and
+// every bf16 x with |x| <= amax: the quantizer's code of x at the tile scale amax / 448 against
+// the E4M3 code of the IEEE quotient.  Mismatching pairs are counted into *mismatches.
+__global__ void __launch_bounds__(256) fp8_quotient_check_kernel(unsigned long long* mismatches) {
+  const uint32_t abits = blockIdx.x + 1u;
+  const float sc = __fdiv_rn(__uint_as_float(abits << 16), 448.f);
+  const float rc = __frcp_rn(sc);
+  const bool fast = sc >= kFastQuotientMinScale;
+  unsigned int bad = 0;
+  for (uint32_t xb = threadIdx.x; xb <= abits; xb += blockDim.x) {
+    const float xp = __uint_as_float(xb << 16), xn = __uint_as_float((xb | 0x8000u) << 16);
+    const uint16_t got = code_pair(xp, xn, sc, rc, fast);
+    const uint16_t want = pack_e4m3x2(__fdiv_rn(xp, sc), __fdiv_rn(xn, sc));
+    bad += ((got & 0xFFu) != (want & 0xFFu)) + ((got >> 8) != (want >> 8));
+  }
+  #pragma unroll
+  for (int off = 16; off > 0; off >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, off);
+  if ((threadIdx.x & 31) == 0 && bad) atomicAdd(mismatches, static_cast<unsigned long long>(bad));
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quotient_check(unsigned long long* mismatches, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(mismatches, 0, sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  fp8_quotient_check_kernel<<<0x7F7F, 256, 0, stream>>>(mismatches);
   return cudaGetLastError();
 }
 

@@ -71,5 +71,8 @@ struct Fp8Layout {
 cudaError_t launch_fwd_fp8(const Fp8Params& p, bool causal, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scales, int BH, int N, int d,
                                 bool transpose, cudaStream_t stream);
+// Compares the quantizer's codes with those of the IEEE quotient for every bf16 value x and every
+// tile maximum amax >= |x| (attn_selftest_fp8_quotients); the count lands in *mismatches.
+cudaError_t launch_fp8_quotient_check(unsigned long long* mismatches, cudaStream_t stream);
 
 }  // namespace attn

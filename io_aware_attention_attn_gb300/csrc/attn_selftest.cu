@@ -4,6 +4,7 @@
 //   mode 1: D[128 x dim] = A[128 x 128] B[128 x dim]    (A K-major, B MN-major: the P V product)
 //   mode 2: as mode 1 with A held in tensor memory (two bf16 per 32-bit column), written there by
 //           tcgen05.st from the threads' registers: the P V product with P kept on chip
+#include "attn_fp8.h"
 #include "attn_gb300.h"
 #include "attn_host.h"
 #include "sm103_ptx.cuh"
@@ -182,4 +183,15 @@ extern "C" int attn_selftest_wait_timeout(void* stream) {
   if (!status) return ATTN_ERR_LAUNCH;
   wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+extern "C" int attn_selftest_fp8_quotients(unsigned long long* mismatches, void* stream) {
+  using namespace attn;
+  if (!mismatches) return ATTN_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(mismatches) & 7u) return ATTN_ERR_ALIGN;
+  int rc = check_device();
+  if (rc != 0) return rc;
+  return launch_fp8_quotient_check(mismatches, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_LAUNCH;
 }

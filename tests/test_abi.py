@@ -97,6 +97,8 @@ def test_selftest_validation(lib):
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 0, 32, None) == -2
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, 7, 64, None) == -9
     assert lib.attn_selftest_mma(ALIGNED, ALIGNED, ALIGNED, -1, 64, None) == -9
+    assert lib.attn_selftest_fp8_quotients(None, None) == -1
+    assert lib.attn_selftest_fp8_quotients(ALIGNED + 4, None) == -4
 
 
 def test_gqa_validation(lib):

@@ -46,6 +46,13 @@ def test_quantizer_bit_exact(seed, B, H, N, d, sigma):
     assert np.all(ct[..., N:] == 0)
 
 
+def test_quantizer_quotient_equals_ieee_division_for_every_bf16_pair():
+    # every bf16 x against every tile maximum amax >= |x|: the quantizer's multiply-and-correct
+    # quotient must give the code of the correctly rounded division (the oracle's), so the
+    # bit-exact cases above hold for every input, not only the sampled ones
+    assert attn.selftest_fp8_quotients() == 0
+
+
 def test_quantizer_zero_tile_and_negative_underflow():
     x = np.zeros((1, 1, 200, 128), dtype=np.uint16)
     x[0, 0, 150, 3] = 0x3F80            # 1.0 in the second tile
