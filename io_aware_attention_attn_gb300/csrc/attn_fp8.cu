@@ -37,32 +37,40 @@ __device__ __forceinline__ uint16_t code_pair(float x0, float x1, float sc, floa
               : pack_e4m3x2(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
 }
 
-// One block per (head slice z, 128-row tile t); thread 2r + h holds half h of row r.  The tile
-// stays in registers as packed bf16 (D/4 words a thread), every load issued before the first use,
-// so four blocks fit on an SM with their whole tiles (32 KB each at d = 128) in flight.
+// One block per (head slice z, 128-row tile t).  The tile is 128 * D / 8 chunks of 16 bytes (8
+// values); each thread holds D / 16 of them in registers as packed bf16, every load issued before
+// the first use, so four blocks fit on an SM with their whole tiles (32 KB at d = 128) in flight.
+// Row-major codes: thread i takes chunks i, i + 256, ..., so each load instruction of a warp reads
+// 512 contiguous bytes and each store writes 256.  Transposed codes: thread 2r + h takes half h of
+// row r, whose codes it writes down column r of the shared-memory staging tile.
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads, 4) quantize_fp8_kernel(
     const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes, float* __restrict__ scales,
     int N, int n_tiles, int n_pad, int transpose) {
-  constexpr int kPer = D / 2;  // elements per thread: row = tid / 2, half = tid % 2
+  constexpr int kRowChunks = D / 8;                          // chunks per row
+  constexpr int kPer = kBM * kRowChunks / kQuantThreads;     // chunks per thread (D / 16)
   __shared__ float red[kQuantThreads / 32];
   __shared__ float s_scale, s_rcp;
   __shared__ __align__(16) uint8_t tile_t[D][kBM + 16];  // transposed codes (transpose only)
   const int z = blockIdx.x / n_tiles;
   const int t = blockIdx.x % n_tiles;
-  const int r = threadIdx.x >> 1;
-  const int c0 = (threadIdx.x & 1) * kPer;
-  const int row = t * kBM + r;
-  const bool valid = row < N;
-  uint4 w[kPer / 8];  // 8 bf16 values each
-  const __nv_bfloat16* src = x + (static_cast<size_t>(z) * N + (valid ? row : 0)) * D + c0;
+  const int rows = min(kBM, N - t * kBM);  // rows of this tile inside the tensor
+  const size_t base = (static_cast<size_t>(z) * N + static_cast<size_t>(t) * kBM) * D;
+  auto chunk = [&](int i) {
+    return transpose ? (threadIdx.x >> 1) * kRowChunks + (threadIdx.x & 1) * kPer + i
+                     : static_cast<int>(threadIdx.x) + kQuantThreads * i;
+  };
+  uint4 w[kPer];  // 8 bf16 values each
+  const uint4* src = reinterpret_cast<const uint4*>(x + base);
   #pragma unroll
-  for (int i = 0; i < kPer / 8; ++i)
-    w[i] = valid ? reinterpret_cast<const uint4*>(src)[i] : make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < kPer; ++i) {
+    const int k = chunk(i);
+    w[i] = k / kRowChunks < rows ? src[k] : make_uint4(0, 0, 0, 0);
+  }
   // |x| maximum in bf16 (the maximum of bf16 values is one of them: exact)
   __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
   #pragma unroll
-  for (int i = 0; i < kPer / 8; ++i) {
+  for (int i = 0; i < kPer; ++i) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[i]);
     #pragma unroll
     for (int q = 0; q < 4; ++q) m2 = __hmax2(m2, __habs2(h[q]));
@@ -83,29 +91,36 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_fp8_kernel(
   __syncthreads();
   const float sc = s_scale, rc = s_rcp;
   const bool fast = sc >= kFastQuotientMinScale;
-  uint32_t w32[kPer / 4];
+  uint2 cw[kPer];  // the 8 codes of each chunk
   #pragma unroll
-  for (int i = 0; i < kPer / 8; ++i) {
+  for (int i = 0; i < kPer; ++i) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    uint32_t c[2];
     #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const float2 a = __bfloat1622float2(h[2 * q]), b = __bfloat1622float2(h[2 * q + 1]);
-      w32[2 * i + q] = static_cast<uint32_t>(code_pair(a.x, a.y, sc, rc, fast)) |
-                       (static_cast<uint32_t>(code_pair(b.x, b.y, sc, rc, fast)) << 16);
+      c[q] = static_cast<uint32_t>(code_pair(a.x, a.y, sc, rc, fast)) |
+             (static_cast<uint32_t>(code_pair(b.x, b.y, sc, rc, fast)) << 16);
     }
+    cw[i] = make_uint2(c[0], c[1]);
   }
   if (!transpose) {
-    if (valid) {
-      uint4* dst = reinterpret_cast<uint4*>(codes + (static_cast<size_t>(z) * N + row) * D + c0);
-      #pragma unroll
-      for (int i = 0; i < kPer / 16; ++i)
-        dst[i] = make_uint4(w32[4 * i], w32[4 * i + 1], w32[4 * i + 2], w32[4 * i + 3]);
+    uint2* dst = reinterpret_cast<uint2*>(codes + base);
+    #pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int k = chunk(i);
+      if (k / kRowChunks < rows) dst[k] = cw[i];
     }
     return;
   }
   // transposed: stage [d][row] in shared memory, then write 128-byte rows of [d][Npad]
+  const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * (D / 2);
   #pragma unroll
-  for (int i = 0; i < kPer; ++i) tile_t[c0 + i][r] = static_cast<uint8_t>(w32[i >> 2] >> (8 * (i & 3)));
+  for (int i = 0; i < kPer; ++i)
+    #pragma unroll
+    for (int e = 0; e < 8; ++e)
+      tile_t[c0 + 8 * i + e][r] =
+          static_cast<uint8_t>((e < 4 ? cw[i].x : cw[i].y) >> (8 * (e & 3)));
   __syncthreads();
   for (int e = threadIdx.x; e < D * (kBM / 16); e += kQuantThreads) {
     const int c = e / (kBM / 16), seg = e % (kBM / 16);
