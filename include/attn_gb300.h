@@ -204,8 +204,10 @@ ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  * 4 exponent, 3 mantissa bits, largest magnitude 448; per-tile scaling).  For every tile of 128
  * rows of a head of the bf16 tensor x [B, H, N, d] (d = 64 or 128):
  *   scale = amax / 448 in fp32 (1 for an all-zero tile), written to scales[(b*H + h)*T + t]
- *   (T = ceil(N/128)); code = E4M3 round-to-nearest-even of x / scale (fp32 IEEE division),
- *   saturating at +-448, the sign bit kept for values that round to zero.
+ *   (T = ceil(N/128)); code = E4M3 round-to-nearest-even of x / scale rounded to nearest fp32
+ *   (the IEEE quotient, which the kernel forms from the tile's reciprocal with one correction;
+ *   attn_selftest_fp8_quotients checks every input), saturating at +-448, the sign bit kept for
+ *   values that round to zero.
  *   transpose = 0: codes [B, H, N, d] (N*d bytes per head)
  *   transpose = 1: codes [B, H, d, Npad] with Npad = 128*T, padding codes 0 (the V operand of
  *                  attn_fwd_fp8)
