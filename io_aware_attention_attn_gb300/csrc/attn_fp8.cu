@@ -21,9 +21,11 @@ constexpr int kQuantThreads = 256;
 // q0 = RN(x rc), the remainder x - sc q0 is exact under a fused multiply-add and RN(q0 + rem rc)
 // is the rounded quotient (the correction step of FMA-based division: P. Markstein, "Computation
 // of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1),
-// 1990).  The sign comes from x, so -0 stays -0.  Used for the scales of tiles whose reciprocal
-// is far from the fp32 range's ends; attn_selftest_fp8_quotients compares the codes it gives
-// with those of the IEEE division for every bf16 value and every scale a bf16 tile can have.
+// 1990).  The sign comes from x, so -0 stays -0.  For x below fp32's normal range the exact
+// remainder can fall under the subnormal spacing and the quotient lose its last bit, but such
+// quotients code to 0 either way.  Used for the scales of tiles whose reciprocal is far from the
+// fp32 range's ends; attn_selftest_fp8_quotients compares the codes it gives with those of the
+// IEEE division for every bf16 value and every scale a bf16 tile can have.
 constexpr float kFastQuotientMinScale = 0x1p-100f;
 
 __device__ __forceinline__ float quotient_rn(float x, float sc, float rc) {
